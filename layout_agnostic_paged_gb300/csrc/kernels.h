@@ -1,0 +1,41 @@
+// kernels.h -- internal launchers shared by the C-ABI translation unit.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace splash {
+
+// Arguments of one decode-kernel launch (device pointers, already validated).
+struct DecodeArgs {
+    const void* q;              // bf16 [B][H][576]
+    const void* kv_pool;        // bf16 [num_pages][P][576]
+    const int32_t* block_table; // [B][max_pages]
+    float* out;                 // [B][H][512]
+    float* lse;                 // [B][H]
+    void* ws;                   // workspace (plan + partials)
+    int B, H, P, num_pages, max_pages;
+    int head_lo, Hs;            // head slice
+    int num_groups;             // CTA groups G'
+    float scale;
+};
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device).
+cudaError_t ensure_smem_optin(const void* kernel, int bytes);
+
+cudaError_t launch_plan(const int32_t* ctx_lens, int B, int64_t tok_lo, int64_t tok_hi, int max_ctx,
+                        int num_groups, int Hs, void* ws, cudaStream_t stream);
+cudaError_t launch_combine(const void* ws, int B, int H, int head_lo, int Hs, int num_groups,
+                           float* out, float* lse, cudaStream_t stream);
+cudaError_t launch_lse_merge(const float* part_out, const float* part_lse, int S, int64_t rows,
+                             int d_v, float* out, float* lse, cudaStream_t stream);
+cudaError_t launch_kv_migrate(const void* src, void* dst, size_t page_bytes, const int32_t* src_ids,
+                              const int32_t* dst_ids, int n, int src_np, int dst_np, int sm_count,
+                              cudaStream_t stream);
+
+// SIMT decode kernel: heads in groups of kSimtHeads, one CTA per (CTA group, head group).
+constexpr int kSimtHeads = 16;
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace splash

@@ -1,0 +1,243 @@
+// plan_merge.cu -- split-KV plan (K1), intra-call combine of split partials (K3)
+// and the public log-sum-exp merge (K4).
+//
+// The plan balances ragged requests across the persistent decode grid: all
+// requests' 128-token tiles are concatenated and cut into G' equal ranges, one
+// per CTA group; a request cut across several groups yields one partial per
+// group, combined by K3 with the same log-sum-exp merge K4 exposes.  The cut
+// depends only on the context lengths and the token range, never on physical
+// page ids, so results are identical under any page permutation.
+//
+// Method context: "SPLASH: Switching Parallel Layouts of Attention with Seamless
+// Handoff for LLM Serving", Appendix, Table 2 (busiest-rank load of each layout:
+// balance is what the layouts trade; CP reads an equal token share under ideal
+// token partitioning, which is the partial + log-sum-exp merge implemented here).
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace splash {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// Inclusive block scan of one int64 per thread (kPlanThreads threads).
+__device__ int64_t block_inclusive_scan(int64_t v, int64_t* warp_sums) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t s = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t n = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += n;
+        }
+        warp_sums[lane] = s;
+    }
+    __syncthreads();
+    int64_t add = warp > 0 ? warp_sums[warp - 1] : 0;
+    __syncthreads();
+    return v + add;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ ctx_lens,
+                                                            int B, int64_t tok_lo, int64_t tok_hi,
+                                                            int max_ctx, int num_groups, int Hs,
+                                                            uint8_t* __restrict__ ws) {
+    __shared__ int64_t warp_sums[32];
+    __shared__ int64_t s_total;
+    PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
+    const WorkspaceLayout lay(B, Hs, num_groups);
+    ReqPlan* req = reinterpret_cast<ReqPlan*>(ws + lay.req_off);
+
+    const int per = (B + kPlanThreads - 1) / kPlanThreads;
+    const int r0 = threadIdx.x * per;
+    const int r1 = min(B, r0 + per);
+    bool bad = false;
+
+    // Pass 1: clipped ranges and tile counts.
+    int64_t my_tiles = 0;
+    for (int r = r0; r < r1; ++r) {
+        int L = ctx_lens[r];
+        if (L < 0 || L > max_ctx) {
+            bad = true;
+            L = min(max(L, 0), max_ctx);
+        }
+        int64_t lo = tok_lo;
+        int64_t hi = tok_hi < 0 ? int64_t(L) : min(tok_hi, int64_t(L));
+        ReqPlan p;
+        p.ctx_len = L;
+        if (hi <= lo) {
+            p.lo = p.hi = 0;
+            p.tile0 = 0;
+            p.ntiles = 0;
+        } else {
+            p.lo = int32_t(lo);
+            p.hi = int32_t(hi);
+            p.tile0 = int32_t(lo / kTileTokens);
+            p.ntiles = int32_t((hi + kTileTokens - 1) / kTileTokens - lo / kTileTokens);
+        }
+        p.tile_begin = my_tiles;  // thread-local prefix for now
+        p.first_grp = 0;
+        p.nsplit = 0;
+        p.slot_base = -1;
+        p.pad[0] = p.pad[1] = 0;
+        req[r] = p;
+        my_tiles += p.ntiles;
+    }
+    const int64_t incl = block_inclusive_scan(my_tiles, warp_sums);
+    const int64_t excl = incl - my_tiles;
+    if (threadIdx.x == kPlanThreads - 1) s_total = incl;
+    __syncthreads();
+    const int64_t T = s_total;
+
+    // Pass 2: global tile offsets, CTA-group cut and partial-slot counts.
+    int64_t my_slots = 0;
+    for (int r = r0; r < r1; ++r) {
+        ReqPlan& p = req[r];
+        p.tile_begin += excl;
+        if (p.ntiles > 0) {
+            const int64_t g0 = group_of_tile(p.tile_begin, T, num_groups);
+            const int64_t g1 = group_of_tile(p.tile_begin + p.ntiles - 1, T, num_groups);
+            p.first_grp = int32_t(g0);
+            p.nsplit = int32_t(g1 - g0 + 1);
+            if (p.nsplit > 1) my_slots += p.nsplit;
+        }
+    }
+    const int64_t sincl = block_inclusive_scan(my_slots, warp_sums);
+    int64_t slot = sincl - my_slots;
+    for (int r = r0; r < r1; ++r) {
+        ReqPlan& p = req[r];
+        if (p.nsplit > 1) {
+            p.slot_base = int32_t(slot);
+            slot += p.nsplit;
+        }
+    }
+    const bool any_bad = __syncthreads_or(bad);
+    if (threadIdx.x == kPlanThreads - 1) {
+        hdr->status = any_bad ? uint32_t(SPLASH_DEVICE_BAD_INPUT) : 0u;
+        hdr->num_groups = num_groups;
+        hdr->total_tiles = T;
+        hdr->num_reqs = B;
+        hdr->heads = Hs;
+        hdr->max_slots = lay.max_slots;
+        hdr->slots_used = int32_t(sincl);
+    }
+}
+
+// Merge `S` partial rows (out at stride `ostride` floats, lse at stride `lstride`)
+// into one output row; one warp, lanes over d_v in float4 steps.
+__device__ __forceinline__ void warp_lse_merge(const float* __restrict__ pout, int64_t ostride,
+                                               const float* __restrict__ plse, int64_t lstride,
+                                               int S, int d_v, float* __restrict__ out,
+                                               float* __restrict__ lse) {
+    const int lane = threadIdx.x & 31;
+    float m = -INFINITY;
+    for (int s = 0; s < S; ++s) m = fmaxf(m, plse[s * lstride]);
+    if (m == -INFINITY) {
+        for (int j = lane * 4; j < d_v; j += 128)
+            *reinterpret_cast<float4*>(out + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane == 0) *lse = -INFINITY;
+        return;
+    }
+    float wsum = 0.f;
+    for (int s = 0; s < S; ++s) wsum += expf(plse[s * lstride] - m);
+    const float inv = 1.0f / wsum;
+    for (int j = lane * 4; j < d_v; j += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < S; ++s) {
+            const float w = expf(plse[s * lstride] - m);
+            const float4 o = *reinterpret_cast<const float4*>(pout + s * ostride + j);
+            acc.x += w * o.x;
+            acc.y += w * o.y;
+            acc.z += w * o.z;
+            acc.w += w * o.w;
+        }
+        acc.x *= inv;
+        acc.y *= inv;
+        acc.z *= inv;
+        acc.w *= inv;
+        *reinterpret_cast<float4*>(out + j) = acc;
+    }
+    if (lane == 0) *lse = m + logf(wsum);
+}
+
+// K3: one warp per (request, head) of the call's slice.  Requests cut across
+// several CTA groups are merged from the workspace; empty requests get the
+// empty-set result; single-piece requests were written by the decode kernel.
+__global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict__ ws, int B, int H,
+                                                      int head_lo, int Hs, int num_groups,
+                                                      float* __restrict__ out,
+                                                      float* __restrict__ lse) {
+    const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (row >= int64_t(B) * Hs) return;
+    const int r = int(row / Hs), hh = int(row % Hs);
+    const WorkspaceLayout lay(B, Hs, num_groups);
+    const ReqPlan p = reinterpret_cast<const ReqPlan*>(ws + lay.req_off)[r];
+    if (p.nsplit == 1) return;
+    float* o = out + (int64_t(r) * H + head_lo + hh) * kDv;
+    float* l = lse + int64_t(r) * H + head_lo + hh;
+    if (p.nsplit == 0) {
+        const int lane = threadIdx.x & 31;
+        for (int j = lane * 4; j < kDv; j += 128)
+            *reinterpret_cast<float4*>(o + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane == 0) *l = -INFINITY;
+        return;
+    }
+    const float* pout = reinterpret_cast<const float*>(ws + lay.pout_off) +
+                        (int64_t(p.slot_base) * Hs + hh) * kDv;
+    const float* plse = reinterpret_cast<const float*>(ws + lay.plse_off) +
+                        int64_t(p.slot_base) * Hs + hh;
+    warp_lse_merge(pout, int64_t(Hs) * kDv, plse, Hs, p.nsplit, kDv, o, l);
+}
+
+// K4: the public merge, one warp per (b, h) row.
+__global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict__ part_out,
+                                                        const float* __restrict__ part_lse, int S,
+                                                        int64_t rows, int d_v,
+                                                        float* __restrict__ out,
+                                                        float* __restrict__ lse) {
+    const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (row >= rows) return;
+    warp_lse_merge(part_out + row * d_v, rows * d_v, part_lse + row, rows, S, d_v,
+                   out + row * d_v, lse + row);
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* ctx_lens, int B, int64_t tok_lo, int64_t tok_hi, int max_ctx,
+                        int num_groups, int Hs, void* ws, cudaStream_t stream) {
+    plan_kernel<<<1, kPlanThreads, 0, stream>>>(ctx_lens, B, tok_lo, tok_hi, max_ctx, num_groups,
+                                                Hs, static_cast<uint8_t*>(ws));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* ws, int B, int H, int head_lo, int Hs, int num_groups,
+                           float* out, float* lse, cudaStream_t stream) {
+    const int64_t threads = int64_t(B) * Hs * 32;
+    const int blocks = int((threads + 255) / 256);
+    if (blocks == 0) return cudaSuccess;
+    combine_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint8_t*>(ws), B, H, head_lo, Hs,
+                                               num_groups, out, lse);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(const float* part_out, const float* part_lse, int S, int64_t rows,
+                             int d_v, float* out, float* lse, cudaStream_t stream) {
+    const int64_t threads = rows * 32;
+    const int64_t blocks = (threads + 255) / 256;
+    if (blocks == 0) return cudaSuccess;
+    lse_merge_kernel<<<unsigned(blocks), 256, 0, stream>>>(part_out, part_lse, S, rows, d_v, out,
+                                                           lse);
+    return cudaGetLastError();
+}
+
+}  // namespace splash
