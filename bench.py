@@ -1,0 +1,493 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged MLA decode hot path on GB300: KV-tokens/s, with the
+decode kernel's roofline fraction and the fp64 CPU oracle as a baseline.
+
+One step = one pass of every hot-path row over one synthetic batch (by default
+the full-heads workload: B=16, ctx 1,024, 128 query heads, one shared 576-wide
+latent KV head, page 64, shuffled page ids):
+  * CP layout: two token-share decode calls ([0, L/2) and [L/2, L)), each = split
+    plan + tensor-core decode + split combine, producing partial out + LSE;
+  * splash_lse_merge of the two shares into the final out / LSE;
+  * a layout handoff: splash_kv_migrate of 25% of the requests' pages into a
+    second block pool (the migrated requests' block-table rows are prepared once;
+    switching tables is a pointer swap, not a kernel).
+value = KV tokens of the batch / step time (each KV token is read once per step).
+
+Timing: W untimed warm-up steps, then K timed steps; before every step a 512 MB
+buffer is written to flush the 129 MB L2 (outside the timed events); each step
+is bracketed by CUDA events on the launching stream and the K step times are
+summed; ranks meet at a barrier (+ synchronize) before and after and the max
+over ranks is reported.  `--impl reference` times the fp64 C oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn KV-tokens/s; achieved TB/s & TFLOP/s as % of roofline"
+UNIT = "KV-tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="full_heads",
+                    help="tiny | full_heads | cp_long | head_shard | ragged_handoff")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("decode_tc.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "layout_agnostic_paged_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, enabled: bool = True):
+        self.index = index
+        self.proc = None
+        self.path = None
+        self.enabled = enabled
+
+    def __enter__(self):
+        if not self.enabled:
+            return self
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.enabled or self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(f):
+                if len(r) >= 9:
+                    rows.append([x.strip() for x in r])
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- the step
+
+class Step:
+    """Buffers and calls of one step over one batch (see the module docstring).
+
+    The step pattern follows the workload's layout:
+      * CP (tiny, full_heads, cp_long): max(2, token_splits) token-share calls, then
+        splash_lse_merge of the shares;
+      * TP / DOP head shards (head_shard): one call per head shard, rows concatenate;
+      * DP-attention / DOP whole requests (ragged_handoff): one call over the batch.
+    Every pattern ends with the handoff: splash_kv_migrate of migrate_frac (default
+    25%) of the requests' pages into a second pool.
+    """
+
+    def __init__(self, w, inp, device):
+        import torch
+        from layout_agnostic_paged_gb300 import splash as S
+        from layout_agnostic_paged_gb300 import workloads as W
+        self.S = S
+        self.w = w
+        self.inp = inp
+        B, H = w.batch, w.num_heads
+        self.B, self.H = B, H
+        self.out = torch.empty(B, H, 512, device=device)
+        self.lse = torch.empty(B, H, device=device)
+        self.calls = []          # (head_lo, head_hi, tok_lo, tok_hi, out, lse)
+        self.merge = False
+        if w.head_shards > 1:
+            hs = H // w.head_shards
+            for i in range(w.head_shards):
+                self.calls.append((i * hs, (i + 1) * hs, 0, -1, self.out, self.lse))
+            self.pattern = f"{w.head_shards} head-shard calls of {hs} heads"
+        elif w.migrate_frac > 0 and w.token_splits == 1:
+            self.calls.append((0, H, 0, -1, self.out, self.lse))
+            self.pattern = "one whole-request call over the batch"
+        else:
+            n = max(2, w.token_splits)
+            L = max(w.ctx_lens)
+            span = -(-L // n)
+            self.po = torch.empty(n, B, H, 512, device=device)
+            self.pl = torch.empty(n, B, H, device=device)
+            for i in range(n):
+                self.calls.append((0, H, i * span, (i + 1) * span if i + 1 < n else -1,
+                                   self.po[i], self.pl[i]))
+            self.merge = True
+            self.pattern = f"{n} CP token-share calls + LSE merge"
+        hs0 = self.calls[0][1] - self.calls[0][0]
+        self.ws = S.decode_workspace(inp.q, inp.pool, inp.block_table, w.scale, 0, hs0)
+        frac = w.migrate_frac if w.migrate_frac > 0 else 0.25
+        self.mig = W.make_migration(inp, frac, seed=w.seed)
+        self.pool2 = torch.empty((self.mig.dst_num_pages,) + tuple(inp.pool.shape[1:]),
+                                 dtype=inp.pool.dtype, device=device)
+        self.src_ids = self.mig.src_ids.to(device)
+        self.dst_ids = self.mig.dst_ids.to(device)
+        self.pattern += f" + {int(round(100 * frac))}% KV-page handoff ({self.src_ids.numel()} pages)"
+        self.launches_per_step = 3 * len(self.calls) + (1 if self.merge else 0) + 1
+        self.page_bytes = int(inp.pool[0].numel() * inp.pool.element_size())
+
+    def call_algorithmic(self, c):
+        """(bytes, flops) one decode call must move / do."""
+        hl, hh, lo, hi, _, _ = c
+        Hs = hh - hl
+        toks = pages = 0
+        P = self.w.page_size
+        for L in self.w.ctx_lens:
+            a, b = lo, (L if hi < 0 else min(hi, L))
+            if b > a:
+                toks += b - a
+                pages += (b - 1) // P - a // P + 1
+        rows = self.B * Hs
+        return algorithmic(Hs, toks, rows, pages)
+
+    def decode(self, c, q=None, bt=None, ctx=None):
+        inp = self.inp
+        hl, hh, lo, hi, out, lse = c
+        self.S.splash_decode_attn(q if q is not None else inp.q, inp.pool,
+                                  bt if bt is not None else inp.block_table,
+                                  ctx if ctx is not None else inp.ctx_lens, hl, hh, lo, hi,
+                                  out, lse, self.ws, self.w.scale)
+
+    def run(self, q=None, bt=None, ctx=None, decode_events=None):
+        for i, c in enumerate(self.calls):
+            if decode_events is not None:
+                decode_events[i][0].record()
+            self.decode(c, q, bt, ctx)
+            if decode_events is not None:
+                decode_events[i][1].record()
+        if self.merge:
+            self.S.splash_lse_merge(self.po, self.pl, self.out, self.lse)
+        self.S.splash_kv_migrate(self.inp.pool, self.pool2, self.src_ids, self.dst_ids)
+
+    def migrate_bytes(self):
+        return 2 * self.page_bytes * int(self.src_ids.numel())
+
+
+def algorithmic(Hs, tokens_in_call, rows, pages):
+    """Bytes and flops one decode call must move / do: every KV token once (576 bf16),
+    q rows (576 bf16), fp32 out rows + lse, 4 bytes per page id."""
+    bytes_ = tokens_in_call * 576 * 2 + rows * 576 * 2 + rows * (512 * 4 + 4) + pages * 4
+    flops = 2.0 * tokens_in_call * Hs * (576 + 512)
+    return bytes_, flops
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_ours(args, world, rank, local):
+    import torch
+    from layout_agnostic_paged_gb300 import splash as S
+    from layout_agnostic_paged_gb300 import workloads as W
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    S.load_library()
+    w = W.ALL[args.workload]()
+    # weak scaling: every rank owns its own batch of the workload (own seed)
+    inp = W.make_decode_inputs(w.ctx_lens, w.num_heads, w.page_size, w.seed + 1000 * rank,
+                               device=device, spare_frac=w.spare_frac)
+    step = Step(w, inp, device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    K, Wm = args.steps, args.warmup
+
+    for _ in range(Wm):
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    dec_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in step.calls] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local, enabled=not args.no_clocks) as clk:
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record(stream)
+            step.run(decode_events=dec_ev[k])
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    dec_ms = [a.elapsed_time(b) for k in range(K) for a, b in dec_ev[k]]
+    total_ms = max_over_ranks(sum(step_ms), world, device)
+    status = S.splash_workspace_status(step.ws)
+    if status != 0:
+        raise RuntimeError(f"device status word set: {status}")
+
+    # end to end through the public API with host buffers: pinned q / block table /
+    # context lengths copied in, merged out / lse copied back, every step
+    q_h = inp.q.cpu().pin_memory()
+    bt_h = inp.block_table.cpu().pin_memory()
+    ctx_h = inp.ctx_lens.cpu().pin_memory()
+    q_d, bt_d, ctx_d = torch.empty_like(inp.q), torch.empty_like(inp.block_table), torch.empty_like(inp.ctx_lens)
+    out_h = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
+    lse_h = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + ctx_h.numel() * 4
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    e2e_ms = []
+    for k in range(Wm + K):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        ctx_d.copy_(ctx_h, non_blocking=True)
+        step.run(q=q_d, bt=bt_d, ctx=ctx_d)
+        out_h.copy_(step.out, non_blocking=True)
+        lse_h.copy_(step.lse, non_blocking=True)
+        stream.synchronize()
+        if k >= Wm:
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_total = max_over_ranks(sum(e2e_ms), world, device)
+
+    tokens = w.kv_tokens
+    total_tokens = sum_over_ranks(float(tokens), world, device)
+    value = total_tokens * K / (total_ms / 1e3)
+    e2e_value = total_tokens * K / (e2e_total / 1e3)
+
+    # roofline of the dominant kernel: the decode call (plan + tcgen05 decode + combine)
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    call_bytes = [step.call_algorithmic(c) for c in step.calls]
+    alg_bytes = sum(b for b, _ in call_bytes) / len(call_bytes)
+    alg_flops = sum(f for _, f in call_bytes) / len(call_bytes)
+    dec_avg_s = statistics.mean(dec_ms) / 1e3
+    achieved_gbs = alg_bytes / dec_avg_s / 1e9
+    achieved_tfs = alg_flops / dec_avg_s / 1e12
+    traffic = ncu_traffic(args.workload)
+    clocks = clk.summary()
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(w, inp, args.cpu_seconds)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": Wm, "ms_per_step": total_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": w.name, "global_batch": w.batch * world, "seq_len": max(w.ctx_lens),
+                "heads": w.num_heads, "page_size": w.page_size, "kv_tokens_per_rank": tokens,
+                "parallelism": f"replicas{world}" if world > 1 else "single",
+                "step": step.pattern,
+                "l2": "512 MB flush write before every timed step",
+            },
+            "clocks": clocks,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_total / K},
+            "gpu_launches": step.launches_per_step * K,
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": achieved_gbs / hbm_peak, "traffic": traffic,
+                         "kernel": "splash_decode_attn (plan + tcgen05 decode + combine), avg per call",
+                         "alg_bytes_per_launch": alg_bytes, "launch_us": dec_avg_s * 1e6,
+                         "peak_source": f"{peak_src} hbm_gbs",
+                         "tflops": achieved_tfs, "tensor_frac_of_bf16_peak": achieved_tfs / (bf16_peak)},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    return line
+
+
+def cpu_baseline(w, inp, seconds: float):
+    """The fp64 oracle, as it stands, on this host's cores over a bounded sample of the
+    same workload (whole requests, all heads), in KV-tokens/s."""
+    import numpy as np
+    import oracle
+    q = oracle.bf16_bits(inp.q)
+    pool = oracle.bf16_bits(inp.pool)
+    bt = inp.block_table.cpu().numpy()
+    ctx = inp.ctx_lens.cpu().numpy()
+    B = len(ctx)
+    # grow the sample (requests, cycling) until it takes about `seconds`
+    t_total, toks, n = 0.0, 0, 0
+    r = 0
+    while t_total < seconds and n < 10 * B:
+        t0 = time.perf_counter()
+        oracle.decode_attn(q[r:r + 1], pool, bt[r:r + 1], ctx[r:r + 1], w.scale)
+        t_total += time.perf_counter() - t0
+        toks += int(ctx[r])
+        n += 1
+        r = (r + 1) % B
+    return {"value": toks / t_total, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} whole requests (all {w.num_heads} heads, cycling over the batch), "
+                      f"{toks} KV tokens, {t_total:.1f} s"}
+
+
+def run_reference(args, world, rank, local):
+    """The fp64 C oracle as the reference arm, timed on the host cores."""
+    if rank != 0:
+        return None
+    import torch
+    import oracle
+    from layout_agnostic_paged_gb300 import workloads as W
+    w = W.ALL[args.workload]()
+    inp = W.make_decode_inputs(w.ctx_lens, w.num_heads, w.page_size, w.seed, device="cpu"
+                               if w.kv_tokens <= 2_000_000 else "cuda:0", spare_frac=w.spare_frac)
+    q = oracle.bf16_bits(inp.q)
+    pool = oracle.bf16_bits(inp.pool)
+    bt = inp.block_table.cpu().numpy()
+    ctx = inp.ctx_lens.cpu().numpy()
+    # each step: a bounded sample of whole requests (all heads) sized so that
+    # warm-up + steps stay within a few minutes
+    t0 = time.perf_counter()
+    oracle.decode_attn(q[:1], pool, bt[:1], ctx[:1], w.scale)
+    per_req = max(time.perf_counter() - t0, 1e-3)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_req = max(1, min(len(ctx), int(budget / per_req)))
+    times, toks = [], int(ctx[:n_req].sum())
+    for k in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.decode_attn(q[:n_req], pool, bt[:n_req], ctx[:n_req], w.scale)
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = toks * args.steps / total
+    sample = f"{n_req} of {len(ctx)} requests (all {w.num_heads} heads) per step, {toks} KV tokens"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "global_batch": w.batch,
+                                        "seq_len": max(w.ctx_lens), "heads": w.num_heads,
+                                        "page_size": w.page_size},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank, int(os.environ.get("LOCAL_RANK", "0")))
+        return
+    world, rank, local = dist_setup(args)
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,603 @@
+// decode_tc.cu -- tensor-core (tcgen05 / TMEM / TMA) paged MLA decode kernel for sm_103a.
+//
+// Method: "SPLASH: Switching Parallel Layouts of Attention with Seamless Handoff
+// for LLM Serving".  Abstract: with one shared latent KV head, every query head
+// of a request reads the same KV stream, so decode attention over a head share,
+// a token share or whole requests is one contraction over the same paged cache
+// (Appendix, Table 2 gives which share each layout owns).
+//
+// Shape of the contraction per 128-token tile (swap-AB: tokens are the MMA M):
+//   S^T [128 tok x N heads] = K_tile [128 x 576] . Q^T          (36 MMAs, K-major A and B)
+//   softmax over tokens per head (fp32, exp2 domain, lazily rescaled running max)
+//   O^T [512 dv x N heads] += V_tile^T [512 x 128] . P^T [128 x N]  (4 dv blocks x 8 MMAs,
+//                                                                   MN-major A and B)
+// N = heads of the CTA's head group padded to 16/32/64, so S^T (N columns) and
+// O^T (4N columns) fit in the 512 TMEM columns of one SM.  V is the latent
+// prefix of the key: the same shared-memory tile feeds both contractions.
+//
+// Roles (192 threads, one CTA per SM, persistent over the split plan's pieces):
+//   warp 0      TMA producer: Q of the piece, then per tile four 32 KB "pairs"
+//               (latent column blocks 2j, 2j+1) and the 16 KB rope block, each page
+//               fetched through the block table (2D tiled loads, 128-byte swizzle)
+//   warp 1      TMEM allocation and the single MMA-issuing thread
+//   warps 2-5   softmax (S^T from TMEM -> P^T bf16 into the rope slot), zeroing of
+//               V rows past the context (poisoned tails never reach the tensor
+//               core), O rescale, and the epilogue (O^T / l -> out or a partial)
+// Every wait is bounded (see common.cuh); a timeout sets the workspace status
+// bit and the CTA unwinds.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace splash {
+namespace {
+
+constexpr int kWarps = 6;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kSoftmaxBarrier = 1;             // named barrier id of warps 2-5
+constexpr int kColBlockBytes = kTileTokens * 128;  // one 64-column block of a tile: 16 KB
+constexpr int kPairBytes = 2 * kColBlockBytes;
+constexpr float kTau = 8.0f;                   // rescale only when a score beats the max by 2^8
+
+template <int NPAD>
+struct TcConfig {
+    static constexpr int kPairs = NPAD == 64 ? 4 : 5;      // pair slots (ring)
+    static constexpr int kRopes = NPAD == 16 ? 2 : 1;      // rope / P^T slots (ring)
+    static constexpr int kQBytes = 9 * NPAD * 128;
+    static constexpr int kQOff = 0;
+    static constexpr int kPairOff = kQOff + kQBytes;
+    static constexpr int kRopeOff = kPairOff + kPairs * kPairBytes;
+    static constexpr int kBarOff = kRopeOff + kRopes * kColBlockBytes;
+    static constexpr int kNumBars = 2 * kPairs + 2 * kRopes + 7;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    // misc: tmem slot (16 B), abort flag (16 B), m[NPAD], m_new[NPAD], alpha[NPAD], red[4][NPAD]
+    static constexpr int kMiscBytes = 32 + 7 * NPAD * 4;
+    static constexpr int kSmemBytes = kMiscOff + kMiscBytes + 1024;  // + alignment slack
+    static constexpr int kTmemCols = NPAD == 16 ? 128 : (NPAD == 32 ? 256 : 512);
+    static constexpr int kOCol = 0;
+    static constexpr int kSCol = 4 * NPAD;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kSCol + NPAD <= kTmemCols, "TMEM budget");
+};
+
+struct TcParams {
+    DecodeArgs a;
+    float c_log2;        // scale * log2(e): scores in the exp2 domain
+    int group_heads;     // Gs: heads per head group (the last group may have fewer)
+    int head_groups;     // NG
+};
+
+// Smallest r with tile_begin[r] + ntiles[r] > x.
+__device__ __forceinline__ int first_request_after(const ReqPlan* req, int B, int64_t x) {
+    int lo = 0, hi = B;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (req[mid].tile_begin + req[mid].ntiles > x) hi = mid;
+        else lo = mid + 1;
+    }
+    return lo;
+}
+
+struct Piece {
+    int r;
+    int t_lo, t_hi;   // tiles of the request (relative to its first tile)
+    int split;
+    bool valid;
+};
+
+// Iterates the pieces (request, tile range) of CTA group j, identically in every role.
+struct PieceIter {
+    const ReqPlan* req;
+    int B;
+    int64_t aj, bj;
+    int r;
+    int j;
+    __device__ PieceIter(const ReqPlan* req_, int B_, int64_t aj_, int64_t bj_, int j_)
+        : req(req_), B(B_), aj(aj_), bj(bj_), j(j_) {
+        r = (aj < bj) ? first_request_after(req, B, aj) : B;
+    }
+    __device__ bool next(Piece& pc, ReqPlan& p) {
+        while (r < B && req[r].tile_begin < bj) {
+            p = req[r];
+            const int cur = r++;
+            if (p.ntiles == 0) continue;
+            pc.r = cur;
+            pc.t_lo = int(max(aj, p.tile_begin) - p.tile_begin);
+            pc.t_hi = int(min(bj, p.tile_begin + p.ntiles) - p.tile_begin);
+            pc.split = j - p.first_grp;
+            pc.valid = true;
+            return true;
+        }
+        return false;
+    }
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Bounded wait by a whole warp; every lane gets the same verdict.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi, float& rlo, float& rhi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    rlo = __low2float(v);
+    rhi = __high2float(v);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int NPAD>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap map_q,
+                         const __grid_constant__ CUtensorMap map_kv, const TcParams prm) {
+    using C = TcConfig<NPAD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sQ = smem + C::kQOff;
+    uint8_t* sPair = smem + C::kPairOff;
+    uint8_t* sRope = smem + C::kRopeOff;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* pair_full = bars;
+    uint64_t* pair_empty = bars + C::kPairs;
+    uint64_t* rope_full = bars + 2 * C::kPairs;
+    uint64_t* rope_empty = rope_full + C::kRopes;
+    uint64_t* q_full = rope_empty + C::kRopes;
+    uint64_t* q_empty = q_full + 1;
+    uint64_t* s_full = q_full + 2;
+    uint64_t* p_full = q_full + 3;
+    uint64_t* o_full = q_full + 4;
+    uint64_t* o_free = q_full + 5;
+    uint64_t* drain = q_full + 6;
+    uint8_t* misc = smem + C::kMiscOff;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 16);
+    float* sm_m = reinterpret_cast<float*>(misc + 32);
+    float* sm_mnew = sm_m + NPAD;
+    float* sm_alpha = sm_mnew + NPAD;
+    float* sm_red = sm_alpha + NPAD;  // [4][NPAD]
+
+    const DecodeArgs& a = prm.a;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
+    uint32_t* status = &hdr->status;
+    const WorkspaceLayout lay(a.B, a.Hs, a.num_groups);
+    const ReqPlan* req = reinterpret_cast<const ReqPlan*>(ws + lay.req_off);
+
+    const int NG = prm.head_groups;
+    const int j = blockIdx.x / NG, g = blockIdx.x % NG;
+    const int64_t T = hdr->total_tiles;
+    const int64_t aj = T > 0 ? group_start(j, T, a.num_groups) : 0;
+    const int64_t bj = T > 0 ? group_start(j + 1, T, a.num_groups) : 0;
+    const int hbase = g * prm.group_heads;                  // first head of the group in the slice
+    const int nh = min(prm.group_heads, a.Hs - hbase);      // valid heads of the group
+    const int P = a.P;
+    const int pages_per_tile = kTileTokens / P;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kPairs; ++i) {
+            mbar_init(&pair_full[i], 1);
+            mbar_init(&pair_empty[i], 1);
+        }
+        for (int i = 0; i < C::kRopes; ++i) {
+            mbar_init(&rope_full[i], 1);
+            mbar_init(&rope_empty[i], 1);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_full, kSoftmaxThreads);
+        mbar_init(o_full, 1);
+        mbar_init(o_free, kSoftmaxThreads);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        // The whole warp walks the schedule (so it stays converged); lane 0 issues.
+        if (aj < bj) {
+            if (lane == 0) {
+                prefetch_tensormap(&map_q);
+                prefetch_tensormap(&map_kv);
+            }
+            const uint64_t pol_kv = policy_evict_first();
+            const uint64_t pol_q = policy_evict_last();
+            int ps = 0, pph = 0, rs = 0, rph = 0, qph = 0;
+            PieceIter it(req, a.B, aj, bj, j);
+            Piece pc;
+            ReqPlan p;
+            bool ok = true;
+            while (ok && it.next(pc, p)) {
+                if (!warp_wait(q_empty, qph ^ 1, abort_flag, status)) { ok = false; break; }
+                qph ^= 1;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(q_full, C::kQBytes);
+                    const int qrow = pc.r * a.H + a.head_lo + hbase;
+                    for (int cb = 0; cb < 9; ++cb)
+                        tma_load_2d(sQ + cb * NPAD * 128, &map_q, q_full, cb * 64, qrow, pol_q);
+                }
+                __syncwarp();
+                const int32_t* bt = a.block_table + int64_t(pc.r) * a.max_pages;
+                for (int t = pc.t_lo; t < pc.t_hi && ok; ++t) {
+                    const int tok0 = (p.tile0 + t) * kTileTokens;
+                    // lane k < pages_per_tile looks up page k of the tile
+                    int my_pid = -1;
+                    bool bad = false;
+                    if (lane < pages_per_tile) {
+                        const int ptok = tok0 + lane * P;
+                        if (ptok < p.ctx_len) {
+                            const int id = bt[ptok / P];
+                            if (id >= 0 && id < a.num_pages) my_pid = id;
+                            else bad = true;
+                        }
+                    }
+                    const uint32_t present = __ballot_sync(0xffffffffu, my_pid >= 0);
+                    if (__any_sync(0xffffffffu, bad) && lane == 0)
+                        atomicOr(status, uint32_t(SPLASH_DEVICE_BAD_INPUT));
+                    const uint32_t blk_bytes = uint32_t(__popc(present)) * P * 128;
+                    for (int jj = 0; jj < 4; ++jj) {
+                        if (!warp_wait(&pair_empty[ps], pph ^ 1, abort_flag, status)) { ok = false; break; }
+                        if (lane == 0) mbar_arrive_expect_tx(&pair_full[ps], 2 * blk_bytes);
+                        __syncwarp();
+                        uint8_t* slot = sPair + ps * kPairBytes;
+                        if (my_pid >= 0)
+                            for (int c2 = 0; c2 < 2; ++c2)
+                                tma_load_2d(slot + c2 * kColBlockBytes + lane * P * 128, &map_kv,
+                                            &pair_full[ps], (2 * jj + c2) * 64, my_pid * P, pol_kv);
+                        __syncwarp();
+                        if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
+                    }
+                    if (!ok) break;
+                    if (!warp_wait(&rope_empty[rs], rph ^ 1, abort_flag, status)) { ok = false; break; }
+                    if (lane == 0) mbar_arrive_expect_tx(&rope_full[rs], blk_bytes);
+                    __syncwarp();
+                    if (my_pid >= 0)
+                        tma_load_2d(sRope + rs * kColBlockBytes + lane * P * 128, &map_kv,
+                                    &rope_full[rs], 8 * 64, my_pid * P, pol_kv);
+                    __syncwarp();
+                    if (++rs == C::kRopes) { rs = 0; rph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // The whole warp walks the schedule; lane 0 issues every tcgen05 instruction.
+        if (aj < bj) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, NPAD, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, NPAD, true, true);
+            const uint32_t s_tmem = tmem + C::kSCol;
+            const uint32_t o_tmem = tmem + C::kOCol;
+            const uint32_t aQ = smem_u32(sQ), aPair = smem_u32(sPair), aRope = smem_u32(sRope);
+            int ps = 0, pph = 0, rs = 0, rph = 0, qph = 0, pfph = 0, ofph = 0;
+            PieceIter it(req, a.B, aj, bj, j);
+            Piece pc;
+            ReqPlan p;
+            bool ok = true;
+            while (ok && it.next(pc, p)) {
+                if (!warp_wait(q_full, qph, abort_flag, status)) { ok = false; break; }
+                qph ^= 1;
+                for (int t = pc.t_lo; t < pc.t_hi; ++t) {
+                    const bool first = (t == pc.t_lo), last = (t + 1 == pc.t_hi);
+                    const int ps0 = ps;
+                    // S^T = K_tile . Q^T over the 512 latent dims (pairs) ...
+                    for (int jj = 0; jj < 4; ++jj) {
+                        if (!warp_wait(&pair_full[ps], pph, abort_flag, status)) { ok = false; break; }
+                        tc_fence_after();
+                        if (lane == 0) {
+                            const uint32_t slot = aPair + ps * kPairBytes;
+#pragma unroll
+                            for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+                                for (int k4 = 0; k4 < 4; ++k4) {
+                                    const uint64_t da =
+                                        smem_desc(slot + c2 * kColBlockBytes + k4 * 32, 16, 1024, 2);
+                                    const uint64_t db =
+                                        smem_desc(aQ + (2 * jj + c2) * NPAD * 128 + k4 * 32, 16, 1024, 2);
+                                    mma_bf16_ss(s_tmem, da, db, idesc_qk, (jj | c2 | k4) != 0);
+                                }
+                        }
+                        __syncwarp();
+                        if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
+                    }
+                    if (!ok) break;
+                    // ... and the 64 rope dims
+                    if (!warp_wait(&rope_full[rs], rph, abort_flag, status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t rslot = aRope + rs * kColBlockBytes;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const uint64_t da = smem_desc(rslot + k4 * 32, 16, 1024, 2);
+                            const uint64_t db = smem_desc(aQ + 8 * NPAD * 128 + k4 * 32, 16, 1024, 2);
+                            mma_bf16_ss(s_tmem, da, db, idesc_qk, 1u);
+                        }
+                        tc_commit(s_full);
+                        if (last) tc_commit(q_empty);
+                    }
+                    __syncwarp();
+                    // O^T += V^T . P^T once the softmax has written P^T into the rope slot
+                    if (!warp_wait(p_full, pfph, abort_flag, status)) { ok = false; break; }
+                    pfph ^= 1;
+                    if (first) {
+                        if (!warp_wait(o_free, ofph ^ 1, abort_flag, status)) { ok = false; break; }
+                        ofph ^= 1;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int pslot = (ps0 + jj) % C::kPairs;
+                            const uint32_t slot = aPair + pslot * kPairBytes;
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t da = smem_desc(slot + kk * 2048, kColBlockBytes, 1024, 2);
+                                const uint64_t db = smem_desc(rslot + kk * 2048, 1024, 1024, 2);
+                                mma_bf16_ss(o_tmem + jj * NPAD, da, db, idesc_pv,
+                                            (!first || kk > 0) ? 1u : 0u);
+                            }
+                            tc_commit(&pair_empty[pslot]);
+                        }
+                        tc_commit(&rope_empty[rs]);
+                        if (last) tc_commit(o_full);
+                    }
+                    __syncwarp();
+                    if (++rs == C::kRopes) { rs = 0; rph ^= 1; }
+                }
+            }
+            // drain: every MMA issued so far has completed before TMEM is released
+            if (lane == 0) tc_commit(drain);
+            __syncwarp();
+            volatile int never = 0;
+            mbar_wait(drain, 0, &never, status);
+            __syncwarp();
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int st = threadIdx.x - 64;              // 0..127
+        const int quad = warp & 3;                    // TMEM lane quadrant of this warp
+        const int row = quad * 32 + lane;             // token row of S^T, dv row of O^T
+        const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        const uint32_t s_tmem = tmem + C::kSCol + lane_off;
+        const uint32_t o_tmem = tmem + C::kOCol + lane_off;
+        const float cl = prm.c_log2;
+        float* pout = reinterpret_cast<float*>(ws + lay.pout_off);
+        float* plse = reinterpret_cast<float*>(ws + lay.plse_off);
+        int sph = 0, ofl = 0, rs = 0;
+        int ps_base = 0;      // pair slot of the tile's pair 0 (mirrors the MMA ring)
+        PieceIter it(req, a.B, aj, bj, j);
+        Piece pc;
+        ReqPlan p;
+        bool ok = aj < bj;
+        while (ok && it.next(pc, p)) {
+            named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+            if (st < NPAD) sm_m[st] = -INFINITY;
+            named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+            float lpart[NPAD];
+#pragma unroll
+            for (int h = 0; h < NPAD; ++h) lpart[h] = 0.f;
+            const int32_t* bt = a.block_table + int64_t(pc.r) * a.max_pages;
+            for (int t = pc.t_lo; t < pc.t_hi; ++t) {
+                const bool first = (t == pc.t_lo);
+                const int tok = (p.tile0 + t) * kTileTokens + row;
+                const bool valid = tok >= p.lo && tok < p.hi;
+                bool in_ctx = tok < p.ctx_len;
+                if (in_ctx) {
+                    const int id = bt[tok / P];
+                    in_ctx = id >= 0 && id < a.num_pages;
+                }
+                bool w = mbar_wait(s_full, sph, abort_flag, status);
+                if (named_barrier_or(kSoftmaxBarrier, kSoftmaxThreads, !w)) { ok = false; break; }
+                sph ^= 1;
+                tc_fence_after();
+                // pass 1: does any valid score exceed the running max by more than tau?
+                float excess = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < NPAD / 16; ++c) {
+                    float s[16];
+                    tmem_ld16(s_tmem + c * 16, s);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) excess = fmaxf(excess, s[e] * cl - sm_m[c * 16 + e]);
+                }
+                if (!valid) excess = -INFINITY;
+                const bool rescale = named_barrier_or(kSoftmaxBarrier, kSoftmaxThreads, excess > kTau);
+                if (rescale) {
+                    // exact column max over the tile's valid tokens
+#pragma unroll
+                    for (int c = 0; c < NPAD / 16; ++c) {
+                        float s[16];
+                        tmem_ld16(s_tmem + c * 16, s);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            float v = valid ? s[e] * cl : -INFINITY;
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                            if (lane == 0) sm_red[quad * NPAD + c * 16 + e] = v;
+                        }
+                    }
+                    named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+                    if (st < NPAD) {
+                        const float mo = sm_m[st];
+                        float mn = fmaxf(fmaxf(sm_red[st], sm_red[NPAD + st]),
+                                         fmaxf(sm_red[2 * NPAD + st], sm_red[3 * NPAD + st]));
+                        mn = fmaxf(mn, mo);
+                        sm_mnew[st] = mn;
+                        sm_alpha[st] = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mn);
+                    }
+                    named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+#pragma unroll
+                    for (int h = 0; h < NPAD; ++h) lpart[h] *= sm_alpha[h];
+                    if (!first) {
+                        // O^T columns are heads: scale column h of every dv block by alpha_h
+                        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                            for (int c = 0; c < NPAD / 16; ++c) {
+                                float o[16];
+                                tmem_ld16(o_tmem + jj * NPAD + c * 16, o);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) o[e] *= sm_alpha[c * 16 + e];
+                                tmem_st16(o_tmem + jj * NPAD + c * 16, o);
+                            }
+                        tmem_wait_st();
+                    }
+                    named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+                    if (st < NPAD) sm_m[st] = sm_mnew[st];
+                    named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+                }
+                // pass 2: P^T row = exp2(s * c - m) as bf16 into the rope slot (MN-major,
+                // 128-byte swizzle: 16-byte chunk ch of row r sits at chunk ch ^ (r & 7))
+                uint8_t* prow = sRope + rs * kColBlockBytes + row * 128;
+#pragma unroll
+                for (int c = 0; c < NPAD / 16; ++c) {
+                    float s[16];
+                    tmem_ld16(s_tmem + c * 16, s);
+                    tmem_wait_ld();
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        float p0 = valid ? ex2_approx(s[e] * cl - sm_m[c * 16 + e]) : 0.f;
+                        float p1 = valid ? ex2_approx(s[e + 1] * cl - sm_m[c * 16 + e + 1]) : 0.f;
+                        float r0, r1;
+                        pk[e / 2] = pack_bf16x2(p0, p1, r0, r1);
+                        lpart[c * 16 + e] += r0;
+                        lpart[c * 16 + e + 1] += r1;
+                    }
+                    const int ch0 = 2 * c, ch1 = 2 * c + 1;
+                    *reinterpret_cast<uint4*>(prow + ((ch0 ^ (row & 7)) << 4)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4*>(prow + ((ch1 ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+                // rows outside the context (or of unreadable pages) hold arbitrary bits:
+                // zero them in the V blocks so 0 * NaN never reaches the accumulator
+                if (!in_ctx) {
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    for (int jj = 0; jj < 4; ++jj) {
+                        uint8_t* slot = sPair + ((ps_base + jj) % C::kPairs) * kPairBytes + row * 128;
+#pragma unroll
+                        for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+                            for (int ch = 0; ch < 8; ++ch)
+                                *reinterpret_cast<uint4*>(slot + c2 * kColBlockBytes + ch * 16) = z;
+                    }
+                }
+                ps_base = (ps_base + 4) % C::kPairs;
+                if (++rs == C::kRopes) rs = 0;
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(p_full);
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- epilogue
+            bool w = mbar_wait(o_full, ofl, abort_flag, status);
+            if (named_barrier_or(kSoftmaxBarrier, kSoftmaxThreads, !w)) { ok = false; break; }
+            ofl ^= 1;
+            tc_fence_after();
+            // l_h = sum over the 128 token lanes of the per-lane partial sums
+#pragma unroll
+            for (int h = 0; h < NPAD; ++h) {
+                float v = lpart[h];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0) sm_red[quad * NPAD + h] = v;
+            }
+            named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+            if (st < NPAD)
+                sm_alpha[st] = 1.0f / (sm_red[st] + sm_red[NPAD + st] + sm_red[2 * NPAD + st] +
+                                       sm_red[3 * NPAD + st]);
+            named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+            float* obase;
+            float* lbase;
+            int64_t hstride;
+            if (p.nsplit == 1) {
+                obase = a.out + (int64_t(pc.r) * a.H + a.head_lo + hbase) * kDv;
+                lbase = a.lse + int64_t(pc.r) * a.H + a.head_lo + hbase;
+            } else {
+                const int64_t slot = p.slot_base + pc.split;
+                obase = pout + (slot * a.Hs + hbase) * kDv;
+                lbase = plse + slot * a.Hs + hbase;
+            }
+            hstride = kDv;
+            for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                for (int c = 0; c < NPAD / 16; ++c) {
+                    float o[16];
+                    tmem_ld16(o_tmem + jj * NPAD + c * 16, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int h = c * 16 + e;
+                        if (h < nh) obase[h * hstride + jj * 128 + row] = o[e] * sm_alpha[h];
+                    }
+                }
+            }
+            if (st < nh) {
+                lbase[st] = (sm_m[st] - log2f(sm_alpha[st])) * 0.69314718055994531f;
+            }
+            tc_fence_before();
+            mbar_arrive(o_free);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int NPAD>
+cudaError_t launch_tc(const CUtensorMap& mq, const CUtensorMap& mkv, const TcParams& prm,
+                      int grid, cudaStream_t stream) {
+    using C = TcConfig<NPAD>;
+    cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(mla_decode_tc_kernel<NPAD>),
+                                      C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    mla_decode_tc_kernel<NPAD><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mkv, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_pad_heads(int group_heads) {
+    return group_heads <= 16 ? 16 : (group_heads <= 32 ? 32 : 64);
+}
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& map_q,
+                             const CUtensorMap& map_kv, int head_groups, int group_heads,
+                             cudaStream_t stream) {
+    TcParams prm;
+    prm.a = a;
+    prm.c_log2 = a.scale * 1.4426950408889634f;
+    prm.group_heads = group_heads;
+    prm.head_groups = head_groups;
+    const int grid = a.num_groups * head_groups;
+    switch (tc_pad_heads(group_heads)) {
+        case 16: return launch_tc<16>(map_q, map_kv, prm, grid, stream);
+        case 32: return launch_tc<32>(map_q, map_kv, prm, grid, stream);
+        default: return launch_tc<64>(map_q, map_kv, prm, grid, stream);
+    }
+}
+
+}  // namespace splash

@@ -34,6 +34,16 @@ cudaError_t launch_kv_migrate(const void* src, void* dst, size_t page_bytes, con
                               const int32_t* dst_ids, int n, int src_np, int dst_np, int sm_count,
                               cudaStream_t stream);
 
+// Tensor-core decode kernel: head groups of at most 64 heads, one CTA per (CTA group,
+// head group), persistent over the plan.  map_q covers q as [B*H rows][576] bf16 with
+// a {64, pad(group_heads)} box; map_kv covers the pool as [num_pages*P rows][576] with
+// a {64, P} box; both use the 128-byte swizzle.
+constexpr int kTcMaxGroupHeads = 64;
+int tc_pad_heads(int group_heads);
+cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& map_q,
+                             const CUtensorMap& map_kv, int head_groups, int group_heads,
+                             cudaStream_t stream);
+
 // SIMT decode kernel: heads in groups of kSimtHeads, one CTA per (CTA group, head group).
 constexpr int kSimtHeads = 16;
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);

@@ -1,6 +1,9 @@
 // splash_api.cu -- the C ABI (include/splash.h): host-side validation, workspace
 // sizing, per-device state and kernel launches.  No allocation, no stream
 // synchronisation (except splash_workspace_status, which is documented to sync).
+#include <stdlib.h>
+#include <string.h>
+
 #include <mutex>
 #include <unordered_map>
 
@@ -45,18 +48,70 @@ int validate_desc(const splash_attn_desc* d) {
     return SPLASH_OK;
 }
 
+// Which decode kernel runs: the tensor-core kernel; the CUDA-core kernel only when
+// SPLASH_DECODE_KERNEL=simt is set in the environment (a GPU cross-check).
+bool use_simt() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("SPLASH_DECODE_KERNEL");
+        v = (e && strcmp(e, "simt") == 0) ? 1 : 0;
+    }
+    return v == 1;
+}
+
 // Launch geometry of the decode kernel for a head slice of Hs heads.
 struct Geometry {
-    int head_groups;  // CTAs per CTA group
+    int head_groups;  // CTAs per CTA group (one per head group)
+    int group_heads;  // heads per head group (the last group may have fewer)
     int num_groups;   // CTA groups G' (the tile sequence is cut into G' ranges)
 };
 
 Geometry decode_geometry(int Hs, int sms) {
     Geometry g;
-    g.head_groups = (Hs + kSimtHeads - 1) / kSimtHeads;
-    g.num_groups = (2 * sms) / g.head_groups;
+    if (use_simt()) {
+        g.head_groups = (Hs + kSimtHeads - 1) / kSimtHeads;
+        g.group_heads = kSimtHeads;
+        g.num_groups = (2 * sms) / g.head_groups;
+    } else {
+        g.head_groups = (Hs + kTcMaxGroupHeads - 1) / kTcMaxGroupHeads;
+        g.group_heads = (Hs + g.head_groups - 1) / g.head_groups;
+        g.num_groups = sms / g.head_groups;  // one persistent CTA per SM
+    }
     if (g.num_groups < 1) g.num_groups = 1;
     return g;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2D bf16 map over [rows][576] with a {64, box_rows} box and the 128-byte swizzle.
+bool encode_rows_576(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {uint64_t(kDqk), rows};
+    cuuint64_t strides[1] = {uint64_t(kDqk) * 2};
+    cuuint32_t box[2] = {64u, box_rows};
+    cuuint32_t es[2] = {1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -153,7 +208,21 @@ int splash_decode_attn(const splash_attn_desc* desc, const void* q, const void* 
     a.Hs = Hs;
     a.num_groups = g.num_groups;
     a.scale = desc->scale;
-    if (launch_decode_simt(a, stream) != cudaSuccess) return SPLASH_ERR_CUDA;
+    if (use_simt()) {
+        if (launch_decode_simt(a, stream) != cudaSuccess) return SPLASH_ERR_CUDA;
+    } else {
+        CUtensorMap mq, mkv;
+        const uint32_t qbox = uint32_t(tc_pad_heads(g.group_heads));
+        if (!encode_rows_576(&mq, q, uint64_t(B) * desc->num_heads, qbox)) return SPLASH_ERR_CUDA;
+        // an empty pool still needs a valid map: point it at the workspace (never read,
+        // every page id is then out of range)
+        const void* kv = desc->num_pages > 0 ? kv_pool : workspace;
+        const uint64_t kv_rows = desc->num_pages > 0 ? uint64_t(desc->num_pages) * desc->page_size
+                                                     : uint64_t(1);
+        if (!encode_rows_576(&mkv, kv, kv_rows, uint32_t(desc->page_size))) return SPLASH_ERR_CUDA;
+        if (launch_decode_tc(a, mq, mkv, g.head_groups, g.group_heads, stream) != cudaSuccess)
+            return SPLASH_ERR_CUDA;
+    }
     if (launch_combine(workspace, B, desc->num_heads, head_lo, Hs, g.num_groups, out, lse, stream) !=
         cudaSuccess)
         return SPLASH_ERR_CUDA;
