@@ -22,7 +22,6 @@ over ranks is reported.  `--impl reference` times the fp64 C oracle instead.
 from __future__ import annotations
 
 import argparse
-import csv
 import hashlib
 import io
 import json
@@ -91,56 +90,88 @@ def ncu_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled every millisecond during the timed
+    region, through NVML (libnvidia-ml via ctypes), in a background thread."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int, enabled: bool = True):
-        self.index = index
-        self.proc = None
-        self.path = None
+    def __init__(self, cuda_index: int, enabled: bool = True):
         self.enabled = enabled
+        self.samples = []
+        self.error = None
+        self.max_mhz = None
+        self._stop = None
+        self._thread = None
+        if not enabled:
+            return
+        try:
+            import ctypes
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            self.h = ctypes.c_void_p()
+            bus = self._pci_bus_id(cuda_index)
+            if bus and self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0:
+                pass
+            elif self.nvml.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.h)) != 0:
+                raise OSError("no NVML handle")
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._fn_reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception as e:  # noqa: BLE001 - reported in the JSON line
+            self.error = f"nvml unavailable: {e}"
+            self.enabled = False
+
+    @staticmethod
+    def _pci_bus_id(i):
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(i)
+            return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        except Exception:  # noqa: BLE001
+            return None
+
+    def sample(self):
+        import ctypes
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0 and \
+                self._fn_reasons(self.h, ctypes.byref(r)) == 0:
+            self.samples.append((c.value, r.value))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.sample()
+            self._stop.wait(0.001)
 
     def __enter__(self):
-        if not self.enabled:
-            return self
-        fd, self.path = tempfile.mkstemp(suffix=".csv")
-        os.close(fd)
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
+        if self.enabled:
+            import threading
+            self._stop = threading.Event()
+            self.sample()
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        if self.enabled:
+            self.sample()
+            self._stop.set()
+            self._thread.join()
 
     def summary(self):
-        if not self.enabled or self.proc is None or not self.path:
-            return None
-        rows = []
-        with open(self.path) as f:
-            for r in csv.reader(f):
-                if len(r) >= 9:
-                    rows.append([x.strip() for x in r])
-        os.unlink(self.path)
-        if not rows:
-            return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "samples": 0, "note": self.error or "no samples"}
+        mhz = [c for c, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if bits & b),
+                "samples": len(self.samples), "source": "nvml"}
 
 
 def dist_setup(args):
@@ -300,40 +331,77 @@ def run_ours(args, world, rank, local):
                                device=device, spare_frac=w.spare_frac)
     step = Step(w, inp, device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream(device)
     K, Wm = args.steps, args.warmup
 
-    for _ in range(Wm):
+    # one eager pass (caches the per-device state), then one CUDA graph per timed step
+    # with in-graph events around every decode call
+    step.run()
+    torch.cuda.synchronize()
+
+    def new_event():
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return None
+
+    graphs, dec_ev = [], []
+    side = torch.cuda.Stream(device)
+    for k in range(max(K, 1)):
+        evs = [(new_event(), new_event()) for _ in step.calls]
+        if any(e is None for pair in evs for e in pair):
+            evs = None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            step.run(decode_events=evs)
+        graphs.append(g)
+        dec_ev.append(evs)
+    stream = torch.cuda.current_stream(device)
+    for k in range(Wm):
         flush.zero_()
-        step.run()
+        graphs[k % len(graphs)].replay()
     torch.cuda.synchronize()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    dec_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in step.calls] for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local, enabled=not args.no_clocks) as clk:
         for k in range(K):
             flush.zero_()
             ev[k][0].record(stream)
-            step.run(decode_events=dec_ev[k])
+            graphs[k].replay()
             ev[k][1].record(stream)
         torch.cuda.synchronize()
     barrier(world)
     step_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    dec_ms = [a.elapsed_time(b) for k in range(K) for a, b in dec_ev[k]]
+    if dec_ev[0] is not None:
+        dec_ms = [a.elapsed_time(b) for k in range(K) for a, b in dec_ev[k]]
+        dec_src = "CUDA events captured inside the step graph around each decode call"
+    else:   # events cannot be captured: time graph replays of single decode calls
+        dec_ms = []
+        for c in step.calls[:2]:
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=side):
+                step.decode(c)
+            for k in range(K):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g1.replay()
+                b.record(stream)
+                torch.cuda.synchronize()
+                dec_ms.append(a.elapsed_time(b))
+        dec_src = "CUDA events around graph replays of one decode call"
     total_ms = max_over_ranks(sum(step_ms), world, device)
     status = S.splash_workspace_status(step.ws)
     if status != 0:
         raise RuntimeError(f"device status word set: {status}")
 
     # end to end through the public API with host buffers: pinned q / block table /
-    # context lengths copied in, merged out / lse copied back, every step
+    # context lengths copied in, the step, merged out / lse copied back, every step
     q_h = inp.q.cpu().pin_memory()
     bt_h = inp.block_table.cpu().pin_memory()
     ctx_h = inp.ctx_lens.cpu().pin_memory()
-    q_d, bt_d, ctx_d = torch.empty_like(inp.q), torch.empty_like(inp.block_table), torch.empty_like(inp.ctx_lens)
+    q_d, bt_d, ctx_d = inp.q, inp.block_table, inp.ctx_lens     # the graphs read these buffers
     out_h = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
     lse_h = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
     h2d = q_h.numel() * 2 + bt_h.numel() * 4 + ctx_h.numel() * 4
@@ -346,7 +414,7 @@ def run_ours(args, world, rank, local):
         q_d.copy_(q_h, non_blocking=True)
         bt_d.copy_(bt_h, non_blocking=True)
         ctx_d.copy_(ctx_h, non_blocking=True)
-        step.run(q=q_d, bt=bt_d, ctx=ctx_d)
+        graphs[k % len(graphs)].replay()
         out_h.copy_(step.out, non_blocking=True)
         lse_h.copy_(step.lse, non_blocking=True)
         stream.synchronize()
@@ -383,7 +451,7 @@ def run_ours(args, world, rank, local):
                 "workload": w.name, "global_batch": w.batch * world, "seq_len": max(w.ctx_lens),
                 "heads": w.num_heads, "page_size": w.page_size, "kv_tokens_per_rank": tokens,
                 "parallelism": f"replicas{world}" if world > 1 else "single",
-                "step": step.pattern,
+                "step": step.pattern + "; captured as one CUDA graph",
                 "l2": "512 MB flush write before every timed step",
             },
             "clocks": clocks,
@@ -392,10 +460,11 @@ def run_ours(args, world, rank, local):
             "gpu_launches": step.launches_per_step * K,
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak,
                          "unit": "GB/s", "frac": achieved_gbs / hbm_peak, "traffic": traffic,
-                         "kernel": "splash_decode_attn (plan + tcgen05 decode + combine), avg per call",
+                         "kernel": "splash_decode_attn call (plan + tcgen05 decode + combine)",
                          "alg_bytes_per_launch": alg_bytes, "launch_us": dec_avg_s * 1e6,
-                         "peak_source": f"{peak_src} hbm_gbs",
-                         "tflops": achieved_tfs, "tensor_frac_of_bf16_peak": achieved_tfs / (bf16_peak)},
+                         "timing": dec_src, "peak_source": f"{peak_src} hbm_gbs",
+                         "tflops": achieved_tfs,
+                         "tensor_frac_of_bf16_peak": achieved_tfs / bf16_peak},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

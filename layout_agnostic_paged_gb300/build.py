@@ -42,16 +42,23 @@ def _stale(target: str, sources: list[str]) -> bool:
     return any(os.path.getmtime(s) > t for s in sources)
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile every .cu under csrc/ and link the shared library; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          out_dir: str | None = None) -> str:
+    """Compile every .cu under csrc/ and link the shared library; returns its path.
+
+    ``extra`` adds nvcc flags (e.g. -DSPLASH_TRACE for the phase-trace build) and
+    ``out_dir`` puts objects and the library somewhere other than _build/.
+    """
+    build_dir = out_dir or BUILD
+    lib = os.path.join(build_dir, "libsplash_gb300.so")
+    os.makedirs(build_dir, exist_ok=True)
     cu = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     deps = _deps()
     extra = list(extra or [])
     jobs = []
     objs = []
     for src in cu:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + deps):
             cmd = [nvcc()] + ARCH + CFLAGS + extra + ["-c", src, "-o", obj]
@@ -67,11 +74,11 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -24,7 +24,7 @@ constexpr int kTileTokens = 128; // token tile of every decode kernel (the MMA M
 // ---------------------------------------------------------------------------
 struct PlanHeader {
     uint32_t status;       // SPLASH_DEVICE_* bits of the last call
-    int32_t num_groups;    // CTA groups G': the concatenated tile sequence is cut in G' ranges
+    int32_t num_groups;    // CTA groups in use: min(G', T); the tile sequence is cut in that many ranges
     int64_t total_tiles;   // T: tiles over all requests
     int32_t num_reqs;
     int32_t heads;         // Hs = head_hi - head_lo
@@ -273,6 +273,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            | (uint32_t(N >> 3) << 17)      // N / 8
            | (uint32_t(M >> 4) << 24);     // M / 16
 }
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while its predecessor on the stream is still running;
+// pdl_wait() blocks until the predecessor grid has completed and its memory is
+// visible (a no-op for an ordinary launch), so every kernel calls it before its
+// first global-memory access.  pdl_trigger() lets the successor start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Named barrier over `count` threads with OR-reduction of a predicate.
 __device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred) {

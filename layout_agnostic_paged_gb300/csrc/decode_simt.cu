@@ -44,6 +44,7 @@ __device__ int first_request_after(const ReqPlan* req, int B, int64_t x) {
 __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SimtSmem& sm = *reinterpret_cast<SimtSmem*>(smem_raw);
+    pdl_wait();
     const int NG = (a.Hs + kHG - 1) / kHG;
     const int j = blockIdx.x / NG, g = blockIdx.x % NG;
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
@@ -54,8 +55,9 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
     float* plse = reinterpret_cast<float*>(ws + lay.plse_off);
 
     const int64_t T = hdr->total_tiles;
-    if (T == 0) return;
-    const int64_t aj = group_start(j, T, a.num_groups), bj = group_start(j + 1, T, a.num_groups);
+    const int G = hdr->num_groups;  // groups in use (<= a.num_groups, <= T)
+    if (T == 0 || j >= G) return;
+    const int64_t aj = group_start(j, T, G), bj = group_start(j + 1, T, G);
     if (aj >= bj) return;
     const int hbase = g * kHG;                       // first head of the group within the slice
     const int nh = min(kHG, a.Hs - hbase);
@@ -181,8 +183,7 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream) {
     const int smem = int(sizeof(SimtSmem));
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(decode_simt_kernel), smem);
     if (e != cudaSuccess) return e;
-    decode_simt_kernel<<<a.num_groups * NG, kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_simt_kernel, dim3(a.num_groups * NG), dim3(kThreads), smem, stream, a);
 }
 
 }  // namespace splash

@@ -114,6 +114,23 @@ struct PieceIter {
     }
 };
 
+// Optional phase trace (compiled in only with -DSPLASH_TRACE): globaltimer stamps
+// per CTA and event slot, read back with splash_trace_read().
+#ifdef SPLASH_TRACE
+constexpr int kTraceSlots = 64;
+constexpr int kTraceCtas = 1024;
+__device__ unsigned long long g_trace[kTraceCtas * kTraceSlots];
+#define TRACE(slot)                                                                   \
+    do {                                                                              \
+        if (blockIdx.x < kTraceCtas && (slot) < kTraceSlots)                          \
+            g_trace[blockIdx.x * kTraceSlots + (slot)] = globaltimer_ns();            \
+    } while (0)
+#else
+#define TRACE(slot) \
+    do {            \
+    } while (0)
+#endif
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -127,10 +144,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi, float& rlo, float& rhi) {
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    rlo = __low2float(v);
-    rhi = __high2float(v);
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
@@ -172,17 +187,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* status = &hdr->status;
     const WorkspaceLayout lay(a.B, a.Hs, a.num_groups);
     const ReqPlan* req = reinterpret_cast<const ReqPlan*>(ws + lay.req_off);
-
     const int NG = prm.head_groups;
     const int j = blockIdx.x / NG, g = blockIdx.x % NG;
-    const int64_t T = hdr->total_tiles;
-    const int64_t aj = T > 0 ? group_start(j, T, a.num_groups) : 0;
-    const int64_t bj = T > 0 ? group_start(j + 1, T, a.num_groups) : 0;
     const int hbase = g * prm.group_heads;                  // first head of the group in the slice
     const int nh = min(prm.group_heads, a.Hs - hbase);      // valid heads of the group
     const int P = a.P;
     const int pages_per_tile = kTileTokens / P;
 
+    // Prologue (overlaps the plan kernel under programmatic dependent launch).
+    if (threadIdx.x == 0) TRACE(0);
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kPairs; ++i) {
             mbar_init(&pair_full[i], 1);
@@ -206,19 +219,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, C::kTmemCols);
         tmem_relinquish();
     }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&map_q);
+        prefetch_tensormap(&map_kv);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    if (threadIdx.x == 0) TRACE(1);
+    pdl_wait();     // the plan (and every earlier kernel on the stream) is complete
+    pdl_trigger();  // the combine grid may start launching
+    if (threadIdx.x == 0) TRACE(2);
+    const int64_t T = hdr->total_tiles;
+    const int G = hdr->num_groups;  // groups in use (<= a.num_groups, <= T)
+    const int64_t aj = (T > 0 && j < G) ? group_start(j, T, G) : 0;
+    const int64_t bj = (T > 0 && j < G) ? group_start(j + 1, T, G) : 0;
+
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // The whole warp walks the schedule (so it stays converged); lane 0 issues.
         if (aj < bj) {
-            if (lane == 0) {
-                prefetch_tensormap(&map_q);
-                prefetch_tensormap(&map_kv);
-            }
             const uint64_t pol_kv = policy_evict_first();
             const uint64_t pol_q = policy_evict_last();
             int ps = 0, pph = 0, rs = 0, rph = 0, qph = 0;
@@ -234,8 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int qrow = pc.r * a.H + a.head_lo + hbase;
                     for (int cb = 0; cb < 9; ++cb)
                         tma_load_2d(sQ + cb * NPAD * 128, &map_q, q_full, cb * 64, qrow, pol_q);
+                    TRACE(3);
                 }
                 __syncwarp();
+                int ttr = 0;
                 const int32_t* bt = a.block_table + int64_t(pc.r) * a.max_pages;
                 for (int t = pc.t_lo; t < pc.t_hi && ok; ++t) {
                     const int tok0 = (p.tile0 + t) * kTileTokens;
@@ -254,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (__any_sync(0xffffffffu, bad) && lane == 0)
                         atomicOr(status, uint32_t(SPLASH_DEVICE_BAD_INPUT));
                     const uint32_t blk_bytes = uint32_t(__popc(present)) * P * 128;
+                    if (lane == 0 && ttr < 3) TRACE(4 + ttr * 3);
                     for (int jj = 0; jj < 4; ++jj) {
                         if (!warp_wait(&pair_empty[ps], pph ^ 1, abort_flag, status)) { ok = false; break; }
                         if (lane == 0) mbar_arrive_expect_tx(&pair_full[ps], 2 * blk_bytes);
@@ -267,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
                     }
                     if (!ok) break;
+                    if (lane == 0 && ttr < 3) TRACE(5 + ttr * 3);
                     if (!warp_wait(&rope_empty[rs], rph ^ 1, abort_flag, status)) { ok = false; break; }
                     if (lane == 0) mbar_arrive_expect_tx(&rope_full[rs], blk_bytes);
                     __syncwarp();
@@ -274,6 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d(sRope + rs * kColBlockBytes + lane * P * 128, &map_kv,
                                     &rope_full[rs], 8 * 64, my_pid * P, pol_kv);
                     __syncwarp();
+                    if (lane == 0 && ttr < 3) TRACE(6 + ttr * 3);
+                    ++ttr;
                     if (++rs == C::kRopes) { rs = 0; rph ^= 1; }
                 }
             }
@@ -295,9 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (ok && it.next(pc, p)) {
                 if (!warp_wait(q_full, qph, abort_flag, status)) { ok = false; break; }
                 qph ^= 1;
+                int ttr = 0;
                 for (int t = pc.t_lo; t < pc.t_hi; ++t) {
                     const bool first = (t == pc.t_lo), last = (t + 1 == pc.t_hi);
                     const int ps0 = ps;
+                    if (lane == 0 && ttr < 3) TRACE(13 + ttr * 5);
                     // S^T = K_tile . Q^T over the 512 latent dims (pairs) ...
                     for (int jj = 0; jj < 4; ++jj) {
                         if (!warp_wait(&pair_full[ps], pph, abort_flag, status)) { ok = false; break; }
@@ -321,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     // ... and the 64 rope dims
                     if (!warp_wait(&rope_full[rs], rph, abort_flag, status)) { ok = false; break; }
+                    if (lane == 0 && ttr < 3) TRACE(14 + ttr * 5);
                     tc_fence_after();
                     const uint32_t rslot = aRope + rs * kColBlockBytes;
                     if (lane == 0) {
@@ -332,11 +363,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_commit(s_full);
                         if (last) tc_commit(q_empty);
+                        if (ttr < 3) TRACE(15 + ttr * 5);
                     }
                     __syncwarp();
                     // O^T += V^T . P^T once the softmax has written P^T into the rope slot
                     if (!warp_wait(p_full, pfph, abort_flag, status)) { ok = false; break; }
                     pfph ^= 1;
+                    if (lane == 0 && ttr < 3) TRACE(16 + ttr * 5);
                     if (first) {
                         if (!warp_wait(o_free, ofph ^ 1, abort_flag, status)) { ok = false; break; }
                         ofph ^= 1;
@@ -357,8 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_commit(&rope_empty[rs]);
                         if (last) tc_commit(o_full);
+                        if (ttr < 3) TRACE(17 + ttr * 5);
                     }
                     __syncwarp();
+                    ++ttr;
                     if (++rs == C::kRopes) { rs = 0; rph ^= 1; }
                 }
             }
@@ -407,6 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (named_barrier_or(kSoftmaxBarrier, kSoftmaxThreads, !w)) { ok = false; break; }
                 sph ^= 1;
                 tc_fence_after();
+                const int ttr = t - pc.t_lo;
+                if (st == 0 && ttr < 3) TRACE(28 + ttr * 4);
                 // pass 1: does any valid score exceed the running max by more than tau?
                 float excess = -INFINITY;
 #pragma unroll
@@ -419,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!valid) excess = -INFINITY;
                 const bool rescale = named_barrier_or(kSoftmaxBarrier, kSoftmaxThreads, excess > kTau);
+                if (st == 0 && ttr < 3) TRACE(29 + ttr * 4);
                 if (rescale) {
                     // exact column max over the tile's valid tokens
 #pragma unroll
@@ -464,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (st < NPAD) sm_m[st] = sm_mnew[st];
                     named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
                 }
+                if (st == 0 && ttr < 3) TRACE(30 + ttr * 4);
                 // pass 2: P^T row = exp2(s * c - m) as bf16 into the rope slot (MN-major,
                 // 128-byte swizzle: 16-byte chunk ch of row r sits at chunk ch ^ (r & 7))
                 uint8_t* prow = sRope + rs * kColBlockBytes + row * 128;
@@ -477,10 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 16; e += 2) {
                         float p0 = valid ? ex2_approx(s[e] * cl - sm_m[c * 16 + e]) : 0.f;
                         float p1 = valid ? ex2_approx(s[e + 1] * cl - sm_m[c * 16 + e + 1]) : 0.f;
-                        float r0, r1;
-                        pk[e / 2] = pack_bf16x2(p0, p1, r0, r1);
-                        lpart[c * 16 + e] += r0;
-                        lpart[c * 16 + e + 1] += r1;
+                        pk[e / 2] = pack_bf16x2(p0, p1);
+                        lpart[c * 16 + e] += p0;       // l from the unrounded fp32 P
+                        lpart[c * 16 + e + 1] += p1;
                     }
                     const int ch0 = 2 * c, ch1 = 2 * c + 1;
                     *reinterpret_cast<uint4*>(prow + ((ch0 ^ (row & 7)) << 4)) =
@@ -506,12 +544,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(p_full);
+                if (st == 0 && ttr < 3) TRACE(31 + ttr * 4);
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
             bool w = mbar_wait(o_full, ofl, abort_flag, status);
             if (named_barrier_or(kSoftmaxBarrier, kSoftmaxThreads, !w)) { ok = false; break; }
             ofl ^= 1;
+            if (st == 0) TRACE(40);
             tc_fence_after();
             // l_h = sum over the 128 token lanes of the per-lane partial sums
 #pragma unroll
@@ -556,11 +596,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(o_free);
+            if (st == 0) TRACE(41);
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) TRACE(42);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
@@ -574,11 +616,23 @@ cudaError_t launch_tc(const CUtensorMap& mq, const CUtensorMap& mkv, const TcPar
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(mla_decode_tc_kernel<NPAD>),
                                       C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    mla_decode_tc_kernel<NPAD><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mkv, prm);
-    return cudaGetLastError();
+    return launch_pdl(mla_decode_tc_kernel<NPAD>, dim3(grid), dim3(kThreads), size_t(C::kSmemBytes),
+                      stream, mq, mkv, prm);
 }
 
 }  // namespace
+
+#ifdef SPLASH_TRACE
+extern "C" __attribute__((visibility("default"))) int splash_trace_read(void* host_dst, size_t bytes) {
+    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
+    return cudaMemcpyFromSymbol(host_dst, g_trace, bytes) == cudaSuccess ? 0 : -1;
+}
+extern "C" __attribute__((visibility("default"))) int splash_trace_clear() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_trace) != cudaSuccess) return -1;
+    return cudaMemset(p, 0, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 int tc_pad_heads(int group_heads) {
     return group_heads <= 16 ? 16 : (group_heads <= 32 ? 32 : 64);

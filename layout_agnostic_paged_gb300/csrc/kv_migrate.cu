@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(kMigThreads) kv_migrate_kernel(
     const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t vec_per_page,
     const int32_t* __restrict__ src_ids, const int32_t* __restrict__ dst_ids, int n, int src_np,
     int dst_np) {
+    pdl_wait();
+    pdl_trigger();
     for (int i = blockIdx.x; i < n; i += gridDim.x) {
         const int s = src_ids[i];
         const int d = dst_ids[i];
@@ -45,10 +47,9 @@ cudaError_t launch_kv_migrate(const void* src, void* dst, size_t page_bytes, con
                               cudaStream_t stream) {
     if (n == 0) return cudaSuccess;
     const int blocks = n < sm_count * 8 ? n : sm_count * 8;
-    kv_migrate_kernel<<<blocks, kMigThreads, 0, stream>>>(
-        static_cast<const uint4*>(src), static_cast<uint4*>(dst), int64_t(page_bytes / 16), src_ids,
-        dst_ids, n, src_np, dst_np);
-    return cudaGetLastError();
+    return launch_pdl(kv_migrate_kernel, dim3(blocks), dim3(kMigThreads), 0, stream,
+                      static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                      int64_t(page_bytes / 16), src_ids, dst_ids, n, src_np, dst_np);
 }
 
 }  // namespace splash

@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                                                             uint8_t* __restrict__ ws) {
     __shared__ int64_t warp_sums[32];
     __shared__ int64_t s_total;
+    pdl_wait();
+    pdl_trigger();  // the decode grid may start its prologue now
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
     const WorkspaceLayout lay(B, Hs, num_groups);
     ReqPlan* req = reinterpret_cast<ReqPlan*>(ws + lay.req_off);
@@ -98,6 +100,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     if (threadIdx.x == kPlanThreads - 1) s_total = incl;
     __syncthreads();
     const int64_t T = s_total;
+    // Never more CTA groups than tiles: every group range is then non-empty, so a
+    // request's pieces are exactly the groups its tiles fall in.
+    const int64_t G = min(int64_t(num_groups), T);
 
     // Pass 2: global tile offsets, CTA-group cut and partial-slot counts.
     int64_t my_slots = 0;
@@ -105,8 +110,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         ReqPlan& p = req[r];
         p.tile_begin += excl;
         if (p.ntiles > 0) {
-            const int64_t g0 = group_of_tile(p.tile_begin, T, num_groups);
-            const int64_t g1 = group_of_tile(p.tile_begin + p.ntiles - 1, T, num_groups);
+            const int64_t g0 = group_of_tile(p.tile_begin, T, G);
+            const int64_t g1 = group_of_tile(p.tile_begin + p.ntiles - 1, T, G);
             p.first_grp = int32_t(g0);
             p.nsplit = int32_t(g1 - g0 + 1);
             if (p.nsplit > 1) my_slots += p.nsplit;
@@ -124,7 +129,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     const bool any_bad = __syncthreads_or(bad);
     if (threadIdx.x == kPlanThreads - 1) {
         hdr->status = any_bad ? uint32_t(SPLASH_DEVICE_BAD_INPUT) : 0u;
-        hdr->num_groups = num_groups;
+        hdr->num_groups = int32_t(G);
         hdr->total_tiles = T;
         hdr->num_reqs = B;
         hdr->heads = Hs;
@@ -177,6 +182,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict_
                                                       int head_lo, int Hs, int num_groups,
                                                       float* __restrict__ out,
                                                       float* __restrict__ lse) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (row >= int64_t(B) * Hs) return;
     const int r = int(row / Hs), hh = int(row % Hs);
@@ -205,6 +212,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
                                                         int64_t rows, int d_v,
                                                         float* __restrict__ out,
                                                         float* __restrict__ lse) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (row >= rows) return;
     warp_lse_merge(part_out + row * d_v, rows * d_v, part_lse + row, rows, S, d_v,
@@ -215,9 +224,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
 
 cudaError_t launch_plan(const int32_t* ctx_lens, int B, int64_t tok_lo, int64_t tok_hi, int max_ctx,
                         int num_groups, int Hs, void* ws, cudaStream_t stream) {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(ctx_lens, B, tok_lo, tok_hi, max_ctx, num_groups,
-                                                Hs, static_cast<uint8_t*>(ws));
-    return cudaGetLastError();
+    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, ctx_lens, B, tok_lo,
+                      tok_hi, max_ctx, num_groups, Hs, static_cast<uint8_t*>(ws));
 }
 
 cudaError_t launch_combine(const void* ws, int B, int H, int head_lo, int Hs, int num_groups,
@@ -225,9 +233,8 @@ cudaError_t launch_combine(const void* ws, int B, int H, int head_lo, int Hs, in
     const int64_t threads = int64_t(B) * Hs * 32;
     const int blocks = int((threads + 255) / 256);
     if (blocks == 0) return cudaSuccess;
-    combine_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint8_t*>(ws), B, H, head_lo, Hs,
-                                               num_groups, out, lse);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, stream,
+                      static_cast<const uint8_t*>(ws), B, H, head_lo, Hs, num_groups, out, lse);
 }
 
 cudaError_t launch_lse_merge(const float* part_out, const float* part_lse, int S, int64_t rows,
@@ -235,9 +242,8 @@ cudaError_t launch_lse_merge(const float* part_out, const float* part_lse, int S
     const int64_t threads = rows * 32;
     const int64_t blocks = (threads + 255) / 256;
     if (blocks == 0) return cudaSuccess;
-    lse_merge_kernel<<<unsigned(blocks), 256, 0, stream>>>(part_out, part_lse, S, rows, d_v, out,
-                                                           lse);
-    return cudaGetLastError();
+    return launch_pdl(lse_merge_kernel, dim3(unsigned(blocks)), dim3(256), 0, stream, part_out,
+                      part_lse, S, rows, d_v, out, lse);
 }
 
 }  // namespace splash
