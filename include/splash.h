@@ -134,6 +134,37 @@ SPLASH_API int splash_decode_attn(const splash_attn_desc* desc, const void* q, c
                        void* workspace, size_t ws_bytes, splash_stream_t stream);
 
 /*
+ * splash_decode_attn without a caller workspace.  This entry point has no
+ * counterpart in the paper; it exists for callers that cannot allocate device
+ * memory at the point where they decode: code inside CUDA stream capture (a
+ * cudaMalloc there is not captured and can invalidate the capture), serving loops
+ * whose memory is owned by another allocator or capped by a fixed budget, and
+ * plugins that are handed only input and output buffers.
+ *
+ * Same arguments, results and errors as splash_decode_attn, minus the workspace:
+ * the scratch is a 32 MiB array inside the library, resident on every GPU that
+ * loads the library until the process exits.  No cudaMalloc, cudaFree or other
+ * allocating routine is called.
+ *   - A shape whose splash_decode_workspace_size exceeds 32 MiB is rejected with
+ *     SPLASH_ERR_WORKSPACE.  With 128 heads on a 152-SM GB300 that is more than
+ *     51 requests per call; a 16-head shard takes up to 868.
+ *   - The first call on a device resolves the array's device address
+ *     (cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last call's
+ *     contents (each call rewrites all of it that it reads).  Calls that may
+ *     overlap on the GPU (different streams, or graphs replayed concurrently)
+ *     race on it: serialise them.
+ *   - The device status word of splash_workspace_status is not reachable for
+ *     this entry point.
+ */
+SPLASH_API int splash_decode_attn_noalloc(const splash_attn_desc* desc, const void* q,
+                                          const void* kv_pool, const int32_t* block_table,
+                                          const int32_t* ctx_lens, int head_lo, int head_hi,
+                                          int64_t tok_lo, int64_t tok_hi, float* out, float* lse,
+                                          splash_stream_t stream);
+
+/*
  * Log-sum-exp merge of S partial results over disjoint token sets (the CP
  * combine; Appendix, Table 2, ideal token partitioning):
  *   m = max_s part_lse[s][b][h], w_s = exp(part_lse[s][b][h] - m),

@@ -24,8 +24,9 @@ SPLASH_ERR_CUDA = -4
 SPLASH_DEVICE_TIMEOUT = 1
 SPLASH_DEVICE_BAD_INPUT = 2
 
-EXPORTED = ("splash_decode_workspace_size", "splash_decode_attn", "splash_lse_merge",
-            "splash_kv_migrate", "splash_workspace_status", "splash_status_string")
+EXPORTED = ("splash_decode_workspace_size", "splash_decode_attn", "splash_decode_attn_noalloc",
+            "splash_lse_merge", "splash_kv_migrate", "splash_workspace_status",
+            "splash_status_string")
 
 
 class SplashError(RuntimeError):
@@ -61,6 +62,8 @@ def load_library(path: str | None = None):
         lib.splash_decode_workspace_size.restype = sz
         lib.splash_decode_attn.argtypes = [dp, vp, vp, vp, vp, i32, i32, i64, i64, vp, vp, vp, sz, vp]
         lib.splash_decode_attn.restype = i32
+        lib.splash_decode_attn_noalloc.argtypes = [dp, vp, vp, vp, vp, i32, i32, i64, i64, vp, vp, vp]
+        lib.splash_decode_attn_noalloc.restype = i32
         lib.splash_lse_merge.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
         lib.splash_lse_merge.restype = i32
         lib.splash_kv_migrate.argtypes = [vp, vp, sz, vp, vp, i32, ctypes.c_int32, ctypes.c_int32, vp]
@@ -141,6 +144,31 @@ def splash_decode_attn(q: torch.Tensor, kv_pool: torch.Tensor, block_table: torc
             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != SPLASH_OK:
         raise SplashError(rc, "splash_decode_attn")
+
+
+def splash_decode_attn_noalloc(q: torch.Tensor, kv_pool: torch.Tensor, block_table: torch.Tensor,
+                               ctx_lens: torch.Tensor, head_lo: int, head_hi: int, tok_lo: int,
+                               tok_hi: int, out: torch.Tensor, lse: torch.Tensor, scale: float,
+                               stream=None) -> None:
+    """splash_decode_attn with the library's own fixed scratch instead of a caller
+    workspace (for callers that cannot allocate device memory where they decode,
+    e.g. under stream capture); see splash.h for its size limit and sharing rules."""
+    _check_cuda(q, kv_pool, block_table, ctx_lens, out, lse)
+    if (q.dtype != torch.bfloat16 or kv_pool.dtype != torch.bfloat16 or out.dtype != torch.float32
+            or lse.dtype != torch.float32 or block_table.dtype != torch.int32
+            or ctx_lens.dtype != torch.int32):
+        raise ValueError("splash_decode_attn_noalloc: dtype mismatch")
+    B, H, _ = q.shape
+    if out.shape != (B, H, 512) or lse.shape != (B, H) or ctx_lens.shape != (B,):
+        raise ValueError("splash_decode_attn_noalloc: shape mismatch")
+    desc = make_desc(q, kv_pool, block_table, scale)
+    with torch.cuda.device(q.device):
+        rc = load_library().splash_decode_attn_noalloc(
+            ctypes.byref(desc), _ptr(q), _ptr(kv_pool), _ptr(block_table), _ptr(ctx_lens),
+            int(head_lo), int(head_hi), int(tok_lo), int(tok_hi), _ptr(out), _ptr(lse),
+            _stream(stream))
+    if rc != SPLASH_OK:
+        raise SplashError(rc, "splash_decode_attn_noalloc")
 
 
 def splash_lse_merge(part_out: torch.Tensor, part_lse: torch.Tensor, out: torch.Tensor,
