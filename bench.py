@@ -292,7 +292,7 @@ class Step:
                                   ctx if ctx is not None else inp.ctx_lens, hl, hh, lo, hi,
                                   out, lse, self.ws, self.w.scale)
 
-    def run(self, q=None, bt=None, ctx=None, decode_events=None):
+    def run(self, q=None, bt=None, ctx=None, decode_events=None, row_events=None):
         for i, c in enumerate(self.calls):
             if decode_events is not None:
                 decode_events[i][0].record()
@@ -300,8 +300,21 @@ class Step:
             if decode_events is not None:
                 decode_events[i][1].record()
         if self.merge:
+            if row_events is not None:
+                row_events["lse_merge"][0].record()
             self.S.splash_lse_merge(self.po, self.pl, self.out, self.lse)
+            if row_events is not None:
+                row_events["lse_merge"][1].record()
+        if row_events is not None:
+            row_events["kv_migrate"][0].record()
         self.S.splash_kv_migrate(self.inp.pool, self.pool2, self.src_ids, self.dst_ids)
+        if row_events is not None:
+            row_events["kv_migrate"][1].record()
+
+    def merge_bytes(self):
+        """Bytes splash_lse_merge must move: every share's fp32 rows read once, one written."""
+        n = self.po.shape[0] if self.merge else 0
+        return (n + 1) * self.B * self.H * (512 * 4 + 4)
 
     def migrate_bytes(self):
         return 2 * self.page_bytes * int(self.src_ids.numel())
@@ -344,17 +357,19 @@ def run_ours(args, world, rank, local):
         except TypeError:
             return None
 
-    graphs, dec_ev = [], []
+    graphs, dec_ev, row_ev = [], [], []
     side = torch.cuda.Stream(device)
     for k in range(max(K, 1)):
         evs = [(new_event(), new_event()) for _ in step.calls]
+        rows = {n: (new_event(), new_event()) for n in ("lse_merge", "kv_migrate")}
         if any(e is None for pair in evs for e in pair):
-            evs = None
+            evs, rows = None, None
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=side):
-            step.run(decode_events=evs)
+            step.run(decode_events=evs, row_events=rows)
         graphs.append(g)
         dec_ev.append(evs)
+        row_ev.append(rows)
     stream = torch.cuda.current_stream(device)
     for k in range(Wm):
         flush.zero_()
@@ -391,6 +406,17 @@ def run_ours(args, world, rank, local):
                 torch.cuda.synchronize()
                 dec_ms.append(a.elapsed_time(b))
         dec_src = "CUDA events around graph replays of one decode call"
+    rows_report = {}
+    if row_ev[0] is not None:
+        mig_us = statistics.mean(row_ev[k]["kv_migrate"][0].elapsed_time(row_ev[k]["kv_migrate"][1])
+                                 for k in range(K)) * 1e3
+        rows_report["kv_migrate"] = {"us": mig_us, "bytes": step.migrate_bytes(),
+                                     "gb_s": step.migrate_bytes() / mig_us / 1e3}
+        if step.merge:
+            mer_us = statistics.mean(row_ev[k]["lse_merge"][0].elapsed_time(row_ev[k]["lse_merge"][1])
+                                     for k in range(K)) * 1e3
+            rows_report["lse_merge"] = {"us": mer_us, "bytes": step.merge_bytes(),
+                                        "gb_s": step.merge_bytes() / mer_us / 1e3}
     total_ms = max_over_ranks(sum(step_ms), world, device)
     status = S.splash_workspace_status(step.ws)
     if status != 0:
@@ -465,6 +491,7 @@ def run_ours(args, world, rank, local):
                          "timing": dec_src, "peak_source": f"{peak_src} hbm_gbs",
                          "tflops": achieved_tfs,
                          "tensor_frac_of_bf16_peak": achieved_tfs / bf16_peak},
+            "other_rows": {k: dict(v, frac_of_hbm=v["gb_s"] / hbm_peak) for k, v in rows_report.items()},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -19,6 +19,7 @@ constexpr int kTileTokens = 128; // token tile of every decode kernel (the MMA M
 // Decode workspace layout (all offsets 256-byte aligned):
 //   [0, 256)                PlanHeader
 //   [256, ...)              ReqPlan[B]
+//   group_first_req         int32 [G']: first request with a tile in CTA group j
 //   partial_out             fp32 [max_slots][Hs][512]
 //   partial_lse             fp32 [max_slots][Hs]
 // ---------------------------------------------------------------------------
@@ -48,12 +49,13 @@ static_assert(sizeof(ReqPlan) == 48, "ReqPlan layout");
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WorkspaceLayout {
-    size_t req_off, pout_off, plse_off, total;
+    size_t req_off, grp_off, pout_off, plse_off, total;
     int max_slots;
     __host__ __device__ WorkspaceLayout(int B, int Hs, int num_groups) {
         max_slots = B + num_groups;
         req_off = 256;
-        pout_off = align256(req_off + sizeof(ReqPlan) * size_t(B));
+        grp_off = align256(req_off + sizeof(ReqPlan) * size_t(B));      // int32 [num_groups]
+        pout_off = align256(grp_off + sizeof(int32_t) * size_t(num_groups));
         plse_off = align256(pout_off + size_t(max_slots) * Hs * kDv * sizeof(float));
         total = align256(plse_off + size_t(max_slots) * Hs * sizeof(float));
     }

@@ -30,17 +30,6 @@ struct SimtSmem {
     float m[kHG], l[kHG], alpha[kHG];
 };
 
-// Smallest r with tile_begin[r] + ntiles[r] > x (requests are in tile order).
-__device__ int first_request_after(const ReqPlan* req, int B, int64_t x) {
-    int lo = 0, hi = B;
-    while (lo < hi) {
-        int mid = (lo + hi) >> 1;
-        if (req[mid].tile_begin + req[mid].ntiles > x) hi = mid;
-        else lo = mid + 1;
-    }
-    return lo;
-}
-
 __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SimtSmem& sm = *reinterpret_cast<SimtSmem*>(smem_raw);
@@ -66,7 +55,8 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
     const uint4* pool = static_cast<const uint4*>(a.kv_pool);
     constexpr int kVecPerRow = kDqk * 2 / 16;         // 72 x 16 B per token row
 
-    for (int r = first_request_after(req, a.B, aj); r < a.B && req[r].tile_begin < bj; ++r) {
+    const int32_t* first_req = reinterpret_cast<const int32_t*>(ws + lay.grp_off);
+    for (int r = first_req[j]; r < a.B && req[r].tile_begin < bj; ++r) {
         const ReqPlan p = req[r];
         if (p.ntiles == 0) continue;
         const int64_t t_lo = max(aj, p.tile_begin) - p.tile_begin;

@@ -69,17 +69,6 @@ struct TcParams {
     int head_groups;     // NG
 };
 
-// Smallest r with tile_begin[r] + ntiles[r] > x.
-__device__ __forceinline__ int first_request_after(const ReqPlan* req, int B, int64_t x) {
-    int lo = 0, hi = B;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (req[mid].tile_begin + req[mid].ntiles > x) hi = mid;
-        else lo = mid + 1;
-    }
-    return lo;
-}
-
 struct Piece {
     int r;
     int t_lo, t_hi;   // tiles of the request (relative to its first tile)
@@ -94,9 +83,10 @@ struct PieceIter {
     int64_t aj, bj;
     int r;
     int j;
-    __device__ PieceIter(const ReqPlan* req_, int B_, int64_t aj_, int64_t bj_, int j_)
+    __device__ PieceIter(const ReqPlan* req_, const int32_t* first_req, int B_, int64_t aj_,
+                         int64_t bj_, int j_)
         : req(req_), B(B_), aj(aj_), bj(bj_), j(j_) {
-        r = (aj < bj) ? first_request_after(req, B, aj) : B;
+        r = (aj < bj) ? first_req[j] : B;
     }
     __device__ bool next(Piece& pc, ReqPlan& p) {
         while (r < B && req[r].tile_begin < bj) {
@@ -144,6 +134,37 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+// Reduce-scatter of NV (16 or 32) values per lane across the 32 lanes of a warp:
+// afterwards lane L holds the max (or sum) over all lanes of value L for NV = 32,
+// and of value (L >> 1) for NV = 16 (lanes 2i and 2i+1 agree).  Each step keeps
+// half of the values and trades the other half with the partner lane, so NV = 32
+// costs 31 shuffles instead of 32 x 5 for separate all-reduces.
+template <int NV, bool MAX>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV], int lane) {
+    static_assert(NV == 16 || NV == 32, "16 or 32 values");
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        const int bit = 16 >> step;
+        const int k = NV >> (step + 1);
+        if (k >= 1) {
+            const bool upper = (lane & bit) != 0;
+#pragma unroll
+            for (int i = 0; i < k; ++i) {
+                const float keep = upper ? v[i + k] : v[i];
+                const float send = upper ? v[i] : v[i + k];
+                const float recv = __shfl_xor_sync(0xffffffffu, send, bit);
+                v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+            }
+        }
+    }
+    float r = v[0];
+    if (NV == 16) {
+        const float o = __shfl_xor_sync(0xffffffffu, r, 1);
+        r = MAX ? fmaxf(r, o) : r + o;
+    }
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -187,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* status = &hdr->status;
     const WorkspaceLayout lay(a.B, a.Hs, a.num_groups);
     const ReqPlan* req = reinterpret_cast<const ReqPlan*>(ws + lay.req_off);
+    const int32_t* first_req = reinterpret_cast<const int32_t*>(ws + lay.grp_off);
     const int NG = prm.head_groups;
     const int j = blockIdx.x / NG, g = blockIdx.x % NG;
     const int hbase = g * prm.group_heads;                  // first head of the group in the slice
@@ -244,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_kv = policy_evict_first();
             const uint64_t pol_q = policy_evict_last();
             int ps = 0, pph = 0, rs = 0, rph = 0, qph = 0;
-            PieceIter it(req, a.B, aj, bj, j);
+            PieceIter it(req, first_req, a.B, aj, bj, j);
             Piece pc;
             ReqPlan p;
             bool ok = true;
@@ -314,9 +336,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, NPAD, true, true);
             const uint32_t s_tmem = tmem + C::kSCol;
             const uint32_t o_tmem = tmem + C::kOCol;
-            const uint32_t aQ = smem_u32(sQ), aPair = smem_u32(sPair), aRope = smem_u32(sRope);
+            // Descriptor bases, computed once: a descriptor for a given start address is the
+            // base plus (byte offset >> 4) in its low field (shared addresses < 256 KB), which
+            // keeps the issue loop to one add per operand.
+            const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, 2);               // Q, K-major
+            const uint64_t dk0 = smem_desc(smem_u32(sPair), 16, 1024, 2);            // K tile, K-major
+            const uint64_t dr0 = smem_desc(smem_u32(sRope), 16, 1024, 2);            // rope, K-major
+            const uint64_t dv0 = smem_desc(smem_u32(sPair), kColBlockBytes, 1024, 2); // V^T, MN-major
+            const uint64_t dp0 = smem_desc(smem_u32(sRope), 1024, 1024, 2);          // P^T, MN-major
             int ps = 0, pph = 0, rs = 0, rph = 0, qph = 0, pfph = 0, ofph = 0;
-            PieceIter it(req, a.B, aj, bj, j);
+            PieceIter it(req, first_req, a.B, aj, bj, j);
             Piece pc;
             ReqPlan p;
             bool ok = true;
@@ -333,17 +362,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!warp_wait(&pair_full[ps], pph, abort_flag, status)) { ok = false; break; }
                         tc_fence_after();
                         if (lane == 0) {
-                            const uint32_t slot = aPair + ps * kPairBytes;
+                            const uint64_t da_s = dk0 + uint64_t(ps) * (kPairBytes >> 4);
+                            const uint64_t db_s = dq0 + uint64_t(jj) * (2 * NPAD * 128 >> 4);
 #pragma unroll
                             for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-                                for (int k4 = 0; k4 < 4; ++k4) {
-                                    const uint64_t da =
-                                        smem_desc(slot + c2 * kColBlockBytes + k4 * 32, 16, 1024, 2);
-                                    const uint64_t db =
-                                        smem_desc(aQ + (2 * jj + c2) * NPAD * 128 + k4 * 32, 16, 1024, 2);
-                                    mma_bf16_ss(s_tmem, da, db, idesc_qk, (jj | c2 | k4) != 0);
-                                }
+                                for (int k4 = 0; k4 < 4; ++k4)
+                                    mma_bf16_ss(s_tmem, da_s + ((c2 * kColBlockBytes + k4 * 32) >> 4),
+                                                db_s + ((c2 * NPAD * 128 + k4 * 32) >> 4), idesc_qk,
+                                                (jj | c2 | k4) != 0);
                         }
                         __syncwarp();
                         if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
@@ -353,14 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!warp_wait(&rope_full[rs], rph, abort_flag, status)) { ok = false; break; }
                     if (lane == 0 && ttr < 3) TRACE(14 + ttr * 5);
                     tc_fence_after();
-                    const uint32_t rslot = aRope + rs * kColBlockBytes;
                     if (lane == 0) {
+                        const uint64_t da_r = dr0 + uint64_t(rs) * (kColBlockBytes >> 4);
 #pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4) {
-                            const uint64_t da = smem_desc(rslot + k4 * 32, 16, 1024, 2);
-                            const uint64_t db = smem_desc(aQ + 8 * NPAD * 128 + k4 * 32, 16, 1024, 2);
-                            mma_bf16_ss(s_tmem, da, db, idesc_qk, 1u);
-                        }
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            mma_bf16_ss(s_tmem, da_r + ((k4 * 32) >> 4),
+                                        dq0 + ((8 * NPAD * 128 + k4 * 32) >> 4), idesc_qk, 1u);
                         tc_commit(s_full);
                         if (last) tc_commit(q_empty);
                         if (ttr < 3) TRACE(15 + ttr * 5);
@@ -376,16 +401,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     if (lane == 0) {
+                        const uint64_t db_p = dp0 + uint64_t(rs) * (kColBlockBytes >> 4);
+#pragma unroll
                         for (int jj = 0; jj < 4; ++jj) {
                             const int pslot = (ps0 + jj) % C::kPairs;
-                            const uint32_t slot = aPair + pslot * kPairBytes;
+                            const uint64_t da_v = dv0 + uint64_t(pslot) * (kPairBytes >> 4);
 #pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t da = smem_desc(slot + kk * 2048, kColBlockBytes, 1024, 2);
-                                const uint64_t db = smem_desc(rslot + kk * 2048, 1024, 1024, 2);
-                                mma_bf16_ss(o_tmem + jj * NPAD, da, db, idesc_pv,
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_bf16_ss(o_tmem + jj * NPAD, da_v + ((kk * 2048) >> 4),
+                                            db_p + ((kk * 2048) >> 4), idesc_pv,
                                             (!first || kk > 0) ? 1u : 0u);
-                            }
                             tc_commit(&pair_empty[pslot]);
                         }
                         tc_commit(&rope_empty[rs]);
@@ -417,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* plse = reinterpret_cast<float*>(ws + lay.plse_off);
         int sph = 0, ofl = 0, rs = 0;
         int ps_base = 0;      // pair slot of the tile's pair 0 (mirrors the MMA ring)
-        PieceIter it(req, a.B, aj, bj, j);
+        PieceIter it(req, first_req, a.B, aj, bj, j);
         Piece pc;
         ReqPlan p;
         bool ok = aj < bj;
@@ -458,19 +483,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool rescale = named_barrier_or(kSoftmaxBarrier, kSoftmaxThreads, excess > kTau);
                 if (st == 0 && ttr < 3) TRACE(29 + ttr * 4);
                 if (rescale) {
-                    // exact column max over the tile's valid tokens
+                    // exact column max over the tile's valid tokens: warp reduce-scatter in
+                    // chunks of up to 32 heads, then the 4 warps through shared memory
+                    constexpr int RS = NPAD < 32 ? NPAD : 32;
 #pragma unroll
-                    for (int c = 0; c < NPAD / 16; ++c) {
-                        float s[16];
-                        tmem_ld16(s_tmem + c * 16, s);
-                        tmem_wait_ld();
+                    for (int h0 = 0; h0 < NPAD; h0 += RS) {
+                        float v[RS];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            float v = valid ? s[e] * cl : -INFINITY;
+                        for (int c = 0; c < RS / 16; ++c) {
+                            float s[16];
+                            tmem_ld16(s_tmem + h0 + c * 16, s);
+                            tmem_wait_ld();
 #pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                            if (lane == 0) sm_red[quad * NPAD + c * 16 + e] = v;
+                            for (int e = 0; e < 16; ++e) v[c * 16 + e] = valid ? s[e] * cl : -INFINITY;
                         }
+                        const float m = warp_reduce_scatter<RS, true>(v, lane);
+                        if (RS == 32) sm_red[quad * NPAD + h0 + lane] = m;
+                        else if ((lane & 1) == 0) sm_red[quad * NPAD + h0 + (lane >> 1)] = m;
                     }
                     named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
                     if (st < NPAD) {
@@ -554,12 +583,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (st == 0) TRACE(40);
             tc_fence_after();
             // l_h = sum over the 128 token lanes of the per-lane partial sums
+            {
+                constexpr int RS = NPAD < 32 ? NPAD : 32;
 #pragma unroll
-            for (int h = 0; h < NPAD; ++h) {
-                float v = lpart[h];
+                for (int h0 = 0; h0 < NPAD; h0 += RS) {
+                    float v[RS];
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) sm_red[quad * NPAD + h] = v;
+                    for (int i = 0; i < RS; ++i) v[i] = lpart[h0 + i];
+                    const float sum = warp_reduce_scatter<RS, false>(v, lane);
+                    if (RS == 32) sm_red[quad * NPAD + h0 + lane] = sum;
+                    else if ((lane & 1) == 0) sm_red[quad * NPAD + h0 + (lane >> 1)] = sum;
+                }
             }
             named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
             if (st < NPAD)
@@ -578,17 +612,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lbase = plse + slot * a.Hs + hbase;
             }
             hstride = kDv;
-            for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
-                for (int c = 0; c < NPAD / 16; ++c) {
+            for (int c = 0; c < NPAD / 16; ++c) {
+                float inv[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) inv[e] = sm_alpha[c * 16 + e];
+                float* ocol = obase + int64_t(c * 16) * hstride + row;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
                     float o[16];
                     tmem_ld16(o_tmem + jj * NPAD + c * 16, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int h = c * 16 + e;
-                        if (h < nh) obase[h * hstride + jj * 128 + row] = o[e] * sm_alpha[h];
-                    }
+                    for (int e = 0; e < 16; ++e)
+                        if (c * 16 + e < nh) ocol[e * hstride + jj * 128] = o[e] * inv[e];
                 }
             }
             if (st < nh) {

@@ -126,7 +126,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
             slot += p.nsplit;
         }
     }
-    const bool any_bad = __syncthreads_or(bad);
+    const bool any_bad = __syncthreads_or(bad);   // also orders the tile_begin updates
+    // First request of every CTA group: smallest r whose tiles reach past the group start,
+    // so a decode CTA finds its first piece with one load instead of a search.
+    int32_t* first_req = reinterpret_cast<int32_t*>(ws + lay.grp_off);
+    for (int64_t j = threadIdx.x; j < G; j += kPlanThreads) {
+        const int64_t x = group_start(j, T, G);
+        int lo = 0, hi = B;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (req[mid].tile_begin + req[mid].ntiles > x) hi = mid;
+            else lo = mid + 1;
+        }
+        first_req[j] = lo;
+    }
     if (threadIdx.x == kPlanThreads - 1) {
         hdr->status = any_bad ? uint32_t(SPLASH_DEVICE_BAD_INPUT) : 0u;
         hdr->num_groups = int32_t(G);
@@ -139,14 +152,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 }
 
 // Merge `S` partial rows (out at stride `ostride` floats, lse at stride `lstride`)
-// into one output row; one warp, lanes over d_v in float4 steps.
+// into one output row; one warp.  Lane s < 32 owns split s's weight (broadcast by
+// shuffles); lanes cover d_v in float4 steps with up to 4 independent loads per
+// split in flight per lane.
 __device__ __forceinline__ void warp_lse_merge(const float* __restrict__ pout, int64_t ostride,
                                                const float* __restrict__ plse, int64_t lstride,
                                                int S, int d_v, float* __restrict__ out,
                                                float* __restrict__ lse) {
     const int lane = threadIdx.x & 31;
     float m = -INFINITY;
-    for (int s = 0; s < S; ++s) m = fmaxf(m, plse[s * lstride]);
+    for (int s0 = 0; s0 < S; s0 += 32)
+        if (s0 + lane < S) m = fmaxf(m, plse[(s0 + lane) * lstride]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (m == -INFINITY) {
         for (int j = lane * 4; j < d_v; j += 128)
             *reinterpret_cast<float4*>(out + j) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -154,23 +172,41 @@ __device__ __forceinline__ void warp_lse_merge(const float* __restrict__ pout, i
         return;
     }
     float wsum = 0.f;
-    for (int s = 0; s < S; ++s) wsum += expf(plse[s * lstride] - m);
+    for (int s0 = 0; s0 < S; s0 += 32)
+        if (s0 + lane < S) wsum += expf(plse[(s0 + lane) * lstride] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     const float inv = 1.0f / wsum;
-    for (int j = lane * 4; j < d_v; j += 128) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < S; ++s) {
-            const float w = expf(plse[s * lstride] - m);
-            const float4 o = *reinterpret_cast<const float4*>(pout + s * ostride + j);
-            acc.x += w * o.x;
-            acc.y += w * o.y;
-            acc.z += w * o.z;
-            acc.w += w * o.w;
+    for (int j0 = 0; j0 < d_v; j0 += 512) {       // 512 floats per pass: 4 float4 per lane
+        float4 acc[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < S; s0 += 32) {
+            const float myw = (s0 + lane < S) ? expf(plse[(s0 + lane) * lstride] - m) : 0.f;
+            const int n = min(32, S - s0);
+#pragma unroll 2
+            for (int t = 0; t < n; ++t) {
+                const float w = __shfl_sync(0xffffffffu, myw, t);
+                const float* src = pout + (s0 + t) * ostride + j0 + lane * 4;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (j0 + lane * 4 + c * 128 < d_v) {
+                        const float4 o = *reinterpret_cast<const float4*>(src + c * 128);
+                        acc[c].x += w * o.x;
+                        acc[c].y += w * o.y;
+                        acc[c].z += w * o.z;
+                        acc[c].w += w * o.w;
+                    }
+                }
+            }
         }
-        acc.x *= inv;
-        acc.y *= inv;
-        acc.z *= inv;
-        acc.w *= inv;
-        *reinterpret_cast<float4*>(out + j) = acc;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int jj = j0 + lane * 4 + c * 128;
+            if (jj < d_v)
+                *reinterpret_cast<float4*>(out + jj) =
+                    make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv);
+        }
     }
     if (lane == 0) *lse = m + logf(wsum);
 }
