@@ -402,16 +402,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     if (lane == 0) {
                         const uint64_t db_p = dp0 + uint64_t(rs) * (kColBlockBytes >> 4);
-#pragma unroll
+                        // kept rolled: the 8-MMA body is fetched once, not 4 times cold
+#pragma unroll 1
                         for (int jj = 0; jj < 4; ++jj) {
                             const int pslot = (ps0 + jj) % C::kPairs;
                             const uint64_t da_v = dv0 + uint64_t(pslot) * (kPairBytes >> 4);
 #pragma unroll
-                            for (int kk = 0; kk < 8; ++kk)
+                            for (int kk = 0; kk < 8; ++kk) {
                                 mma_bf16_ss(o_tmem + jj * NPAD, da_v + ((kk * 2048) >> 4),
                                             db_p + ((kk * 2048) >> 4), idesc_pv,
                                             (!first || kk > 0) ? 1u : 0u);
+                                if (jj == 0 && kk == 0 && ttr < 2) TRACE(43 + ttr * 4);
+                            }
                             tc_commit(&pair_empty[pslot]);
+                            if (jj == 0 && ttr < 2) TRACE(44 + ttr * 4);
+                            if (jj == 1 && ttr < 2) TRACE(45 + ttr * 4);
+                            if (jj == 2 && ttr < 2) TRACE(46 + ttr * 4);
                         }
                         tc_commit(&rope_empty[rs]);
                         if (last) tc_commit(o_full);
@@ -486,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // exact column max over the tile's valid tokens: warp reduce-scatter in
                     // chunks of up to 32 heads, then the 4 warps through shared memory
                     constexpr int RS = NPAD < 32 ? NPAD : 32;
-#pragma unroll
+#pragma unroll 1
                     for (int h0 = 0; h0 < NPAD; h0 += RS) {
                         float v[RS];
 #pragma unroll
@@ -515,8 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < NPAD; ++h) lpart[h] *= sm_alpha[h];
                     if (!first) {
                         // O^T columns are heads: scale column h of every dv block by alpha_h
+#pragma unroll 1
                         for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
+#pragma unroll 1
                             for (int c = 0; c < NPAD / 16; ++c) {
                                 float o[16];
                                 tmem_ld16(o_tmem + jj * NPAD + c * 16, o);
@@ -612,13 +619,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lbase = plse + slot * a.Hs + hbase;
             }
             hstride = kDv;
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < NPAD / 16; ++c) {
                 float inv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) inv[e] = sm_alpha[c * 16 + e];
                 float* ocol = obase + int64_t(c * 16) * hstride + row;
-#pragma unroll
+#pragma unroll 1
                 for (int jj = 0; jj < 4; ++jj) {
                     float o[16];
                     tmem_ld16(o_tmem + jj * NPAD + c * 16, o);
