@@ -15,13 +15,14 @@
 // O^T (4N columns) fit in the 512 TMEM columns of one SM.  V is the latent
 // prefix of the key: the same shared-memory tile feeds both contractions.
 //
-// Roles (192 threads, one CTA per SM, persistent over the split plan's pieces):
+// Roles (one CTA per SM, persistent over the split plan's pieces; 192 threads, or
+// 320 at N = 64 where two softmax warpgroups each own half of the heads):
 //   warp 0      TMA producer: Q of the piece, then per tile four 32 KB "pairs"
 //               (latent column blocks 2j, 2j+1) and the 16 KB rope block, each page
 //               fetched through the block table (2D tiled loads, 128-byte swizzle)
 //   warp 1      TMEM allocation and the single MMA-issuing thread
 //   warps 2-5   softmax (S^T from TMEM -> P^T bf16 into the rope slot), zeroing of
-//               V rows past the context (poisoned tails never reach the tensor
+//   (6-9)       V rows past the context (poisoned tails never reach the tensor
 //               core), O rescale, and the epilogue (O^T / l -> out or a partial)
 // Every wait is bounded (see common.cuh); a timeout sets the workspace status
 // bit and the CTA unwinds.
@@ -33,16 +34,16 @@
 namespace splash {
 namespace {
 
-constexpr int kWarps = 6;
-constexpr int kThreads = kWarps * 32;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kSoftmaxBarrier = 1;             // named barrier id of warps 2-5
+constexpr int kSoftmaxThreads = 128;           // threads of one softmax warpgroup
+constexpr int kSoftmaxBarrier = 1;             // named barrier id of the first warpgroup
 constexpr int kColBlockBytes = kTileTokens * 128;  // one 64-column block of a tile: 16 KB
 constexpr int kPairBytes = 2 * kColBlockBytes;
 constexpr float kTau = 8.0f;                   // rescale only when a score beats the max by 2^8
 
 template <int NPAD>
 struct TcConfig {
+    static constexpr int kSoftmaxGroups = NPAD == 64 ? 2 : 1;  // warpgroups sharing the heads
+    static constexpr int kThreads = 64 + 128 * kSoftmaxGroups;
     static constexpr int kPairs = NPAD == 64 ? 4 : 5;      // pair slots (ring)
     static constexpr int kRopes = NPAD == 16 ? 2 : 1;      // rope / P^T slots (ring)
     static constexpr int kQBytes = 9 * NPAD * 128;
@@ -171,7 +172,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 template <int NPAD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
     mla_decode_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_kv, const TcParams prm) {
     using C = TcConfig<NPAD>;
@@ -230,9 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
         mbar_init(s_full, 1);
-        mbar_init(p_full, kSoftmaxThreads);
+        mbar_init(p_full, kSoftmaxThreads * C::kSoftmaxGroups);
         mbar_init(o_full, 1);
-        mbar_init(o_free, kSoftmaxThreads);
+        mbar_init(o_free, kSoftmaxThreads * C::kSoftmaxGroups);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -437,7 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int st = threadIdx.x - 64;              // 0..127
+        // SWG softmax warpgroups; group wg owns heads [hw0, hw0 + HW) of the head group
+        constexpr int SWG = C::kSoftmaxGroups;
+        constexpr int HW = NPAD / SWG;
+        const int st = (threadIdx.x - 64) & 127;      // 0..127 within the warpgroup
+        const int wg = (threadIdx.x - 64) >> 7;
+        const int hw0 = wg * HW;
+        const int bar = kSoftmaxBarrier + wg;         // named barrier of this warpgroup
         const int quad = warp & 3;                    // TMEM lane quadrant of this warp
         const int row = quad * 32 + lane;             // token row of S^T, dv row of O^T
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
@@ -453,12 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ReqPlan p;
         bool ok = aj < bj;
         while (ok && it.next(pc, p)) {
-            named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
-            if (st < NPAD) sm_m[st] = -INFINITY;
-            named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
-            float lpart[NPAD];
+            named_barrier_sync(bar, kSoftmaxThreads);
+            if (st < HW) sm_m[hw0 + st] = -INFINITY;
+            named_barrier_sync(bar, kSoftmaxThreads);
+            float lpart[HW];
 #pragma unroll
-            for (int h = 0; h < NPAD; ++h) lpart[h] = 0.f;
+            for (int h = 0; h < HW; ++h) lpart[h] = 0.f;
             const int32_t* bt = a.block_table + int64_t(pc.r) * a.max_pages;
             for (int t = pc.t_lo; t < pc.t_hi; ++t) {
                 const bool first = (t == pc.t_lo);
@@ -470,30 +477,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     in_ctx = id >= 0 && id < a.num_pages;
                 }
                 bool w = mbar_wait(s_full, sph, abort_flag, status);
-                if (named_barrier_or(kSoftmaxBarrier, kSoftmaxThreads, !w)) { ok = false; break; }
+                if (named_barrier_or(bar, kSoftmaxThreads, !w)) { ok = false; break; }
                 sph ^= 1;
                 tc_fence_after();
                 const int ttr = t - pc.t_lo;
-                if (st == 0 && ttr < 3) TRACE(28 + ttr * 4);
+                if (threadIdx.x == 64 && ttr < 3) TRACE(28 + ttr * 4);
                 // pass 1: does any valid score exceed the running max by more than tau?
                 float excess = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < NPAD / 16; ++c) {
+                for (int c = 0; c < HW / 16; ++c) {
                     float s[16];
-                    tmem_ld16(s_tmem + c * 16, s);
+                    tmem_ld16(s_tmem + hw0 + c * 16, s);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) excess = fmaxf(excess, s[e] * cl - sm_m[c * 16 + e]);
+                    for (int e = 0; e < 16; ++e)
+                        excess = fmaxf(excess, s[e] * cl - sm_m[hw0 + c * 16 + e]);
                 }
                 if (!valid) excess = -INFINITY;
-                const bool rescale = named_barrier_or(kSoftmaxBarrier, kSoftmaxThreads, excess > kTau);
-                if (st == 0 && ttr < 3) TRACE(29 + ttr * 4);
+                const bool rescale = named_barrier_or(bar, kSoftmaxThreads, excess > kTau);
+                if (threadIdx.x == 64 && ttr < 3) TRACE(29 + ttr * 4);
                 if (rescale) {
                     // exact column max over the tile's valid tokens: warp reduce-scatter in
                     // chunks of up to 32 heads, then the 4 warps through shared memory
-                    constexpr int RS = NPAD < 32 ? NPAD : 32;
+                    constexpr int RS = HW < 32 ? HW : 32;
 #pragma unroll 1
-                    for (int h0 = 0; h0 < NPAD; h0 += RS) {
+                    for (int h0 = hw0; h0 < hw0 + HW; h0 += RS) {
                         float v[RS];
 #pragma unroll
                         for (int c = 0; c < RS / 16; ++c) {
@@ -507,56 +515,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (RS == 32) sm_red[quad * NPAD + h0 + lane] = m;
                         else if ((lane & 1) == 0) sm_red[quad * NPAD + h0 + (lane >> 1)] = m;
                     }
-                    named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
-                    if (st < NPAD) {
-                        const float mo = sm_m[st];
-                        float mn = fmaxf(fmaxf(sm_red[st], sm_red[NPAD + st]),
-                                         fmaxf(sm_red[2 * NPAD + st], sm_red[3 * NPAD + st]));
+                    named_barrier_sync(bar, kSoftmaxThreads);
+                    if (st < HW) {
+                        const int h = hw0 + st;
+                        const float mo = sm_m[h];
+                        float mn = fmaxf(fmaxf(sm_red[h], sm_red[NPAD + h]),
+                                         fmaxf(sm_red[2 * NPAD + h], sm_red[3 * NPAD + h]));
                         mn = fmaxf(mn, mo);
-                        sm_mnew[st] = mn;
-                        sm_alpha[st] = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mn);
+                        sm_mnew[h] = mn;
+                        sm_alpha[h] = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mn);
                     }
-                    named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+                    named_barrier_sync(bar, kSoftmaxThreads);
 #pragma unroll
-                    for (int h = 0; h < NPAD; ++h) lpart[h] *= sm_alpha[h];
+                    for (int h = 0; h < HW; ++h) lpart[h] *= sm_alpha[hw0 + h];
                     if (!first) {
                         // O^T columns are heads: scale column h of every dv block by alpha_h
 #pragma unroll 1
                         for (int jj = 0; jj < 4; ++jj)
 #pragma unroll 1
-                            for (int c = 0; c < NPAD / 16; ++c) {
+                            for (int c = 0; c < HW / 16; ++c) {
                                 float o[16];
-                                tmem_ld16(o_tmem + jj * NPAD + c * 16, o);
+                                tmem_ld16(o_tmem + jj * NPAD + hw0 + c * 16, o);
                                 tmem_wait_ld();
 #pragma unroll
-                                for (int e = 0; e < 16; ++e) o[e] *= sm_alpha[c * 16 + e];
-                                tmem_st16(o_tmem + jj * NPAD + c * 16, o);
+                                for (int e = 0; e < 16; ++e) o[e] *= sm_alpha[hw0 + c * 16 + e];
+                                tmem_st16(o_tmem + jj * NPAD + hw0 + c * 16, o);
                             }
                         tmem_wait_st();
                     }
-                    named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
-                    if (st < NPAD) sm_m[st] = sm_mnew[st];
-                    named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+                    named_barrier_sync(bar, kSoftmaxThreads);
+                    if (st < HW) sm_m[hw0 + st] = sm_mnew[hw0 + st];
+                    named_barrier_sync(bar, kSoftmaxThreads);
                 }
-                if (st == 0 && ttr < 3) TRACE(30 + ttr * 4);
+                if (threadIdx.x == 64 && ttr < 3) TRACE(30 + ttr * 4);
                 // pass 2: P^T row = exp2(s * c - m) as bf16 into the rope slot (MN-major,
                 // 128-byte swizzle: 16-byte chunk ch of row r sits at chunk ch ^ (r & 7))
                 uint8_t* prow = sRope + rs * kColBlockBytes + row * 128;
 #pragma unroll
-                for (int c = 0; c < NPAD / 16; ++c) {
+                for (int c = 0; c < HW / 16; ++c) {
                     float s[16];
-                    tmem_ld16(s_tmem + c * 16, s);
+                    tmem_ld16(s_tmem + hw0 + c * 16, s);
                     tmem_wait_ld();
                     uint32_t pk[8];
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
-                        float p0 = valid ? ex2_approx(s[e] * cl - sm_m[c * 16 + e]) : 0.f;
-                        float p1 = valid ? ex2_approx(s[e + 1] * cl - sm_m[c * 16 + e + 1]) : 0.f;
+                        float p0 = valid ? ex2_approx(s[e] * cl - sm_m[hw0 + c * 16 + e]) : 0.f;
+                        float p1 = valid ? ex2_approx(s[e + 1] * cl - sm_m[hw0 + c * 16 + e + 1]) : 0.f;
                         pk[e / 2] = pack_bf16x2(p0, p1);
                         lpart[c * 16 + e] += p0;       // l from the unrounded fp32 P
                         lpart[c * 16 + e + 1] += p1;
                     }
-                    const int ch0 = 2 * c, ch1 = 2 * c + 1;
+                    const int ch0 = (hw0 >> 3) + 2 * c, ch1 = ch0 + 1;
                     *reinterpret_cast<uint4*>(prow + ((ch0 ^ (row & 7)) << 4)) =
                         make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     *reinterpret_cast<uint4*>(prow + ((ch1 ^ (row & 7)) << 4)) =
@@ -564,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // rows outside the context (or of unreadable pages) hold arbitrary bits:
                 // zero them in the V blocks so 0 * NaN never reaches the accumulator
-                if (!in_ctx) {
+                if (!in_ctx && wg == 0) {
                     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                     for (int jj = 0; jj < 4; ++jj) {
                         uint8_t* slot = sPair + ((ps_base + jj) % C::kPairs) * kPairBytes + row * 128;
@@ -580,33 +589,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(p_full);
-                if (st == 0 && ttr < 3) TRACE(31 + ttr * 4);
+                if (threadIdx.x == 64 && ttr < 3) TRACE(31 + ttr * 4);
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
             bool w = mbar_wait(o_full, ofl, abort_flag, status);
-            if (named_barrier_or(kSoftmaxBarrier, kSoftmaxThreads, !w)) { ok = false; break; }
+            if (named_barrier_or(bar, kSoftmaxThreads, !w)) { ok = false; break; }
             ofl ^= 1;
-            if (st == 0) TRACE(40);
+            if (threadIdx.x == 64) TRACE(40);
             tc_fence_after();
             // l_h = sum over the 128 token lanes of the per-lane partial sums
             {
-                constexpr int RS = NPAD < 32 ? NPAD : 32;
+                constexpr int RS = HW < 32 ? HW : 32;
 #pragma unroll
-                for (int h0 = 0; h0 < NPAD; h0 += RS) {
+                for (int h0 = 0; h0 < HW; h0 += RS) {
                     float v[RS];
 #pragma unroll
                     for (int i = 0; i < RS; ++i) v[i] = lpart[h0 + i];
                     const float sum = warp_reduce_scatter<RS, false>(v, lane);
-                    if (RS == 32) sm_red[quad * NPAD + h0 + lane] = sum;
-                    else if ((lane & 1) == 0) sm_red[quad * NPAD + h0 + (lane >> 1)] = sum;
+                    if (RS == 32) sm_red[quad * NPAD + hw0 + h0 + lane] = sum;
+                    else if ((lane & 1) == 0) sm_red[quad * NPAD + hw0 + h0 + (lane >> 1)] = sum;
                 }
             }
-            named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
-            if (st < NPAD)
-                sm_alpha[st] = 1.0f / (sm_red[st] + sm_red[NPAD + st] + sm_red[2 * NPAD + st] +
-                                       sm_red[3 * NPAD + st]);
-            named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+            named_barrier_sync(bar, kSoftmaxThreads);
+            if (st < HW) {
+                const int h = hw0 + st;
+                sm_alpha[h] = 1.0f / (sm_red[h] + sm_red[NPAD + h] + sm_red[2 * NPAD + h] +
+                                      sm_red[3 * NPAD + h]);
+            }
+            named_barrier_sync(bar, kSoftmaxThreads);
             float* obase;
             float* lbase;
             int64_t hstride;
@@ -620,27 +631,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             hstride = kDv;
 #pragma unroll 1
-            for (int c = 0; c < NPAD / 16; ++c) {
+            for (int c = 0; c < HW / 16; ++c) {
+                const int hc = hw0 + c * 16;
                 float inv[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) inv[e] = sm_alpha[c * 16 + e];
-                float* ocol = obase + int64_t(c * 16) * hstride + row;
+                for (int e = 0; e < 16; ++e) inv[e] = sm_alpha[hc + e];
+                float* ocol = obase + int64_t(hc) * hstride + row;
 #pragma unroll 1
                 for (int jj = 0; jj < 4; ++jj) {
                     float o[16];
-                    tmem_ld16(o_tmem + jj * NPAD + c * 16, o);
+                    tmem_ld16(o_tmem + jj * NPAD + hc, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        if (c * 16 + e < nh) ocol[e * hstride + jj * 128] = o[e] * inv[e];
+                        if (hc + e < nh) ocol[e * hstride + jj * 128] = o[e] * inv[e];
                 }
             }
-            if (st < nh) {
-                lbase[st] = (sm_m[st] - log2f(sm_alpha[st])) * 0.69314718055994531f;
+            if (st < HW && hw0 + st < nh) {
+                const int h = hw0 + st;
+                lbase[h] = (sm_m[h] - log2f(sm_alpha[h])) * 0.69314718055994531f;
             }
             tc_fence_before();
             mbar_arrive(o_free);
-            if (st == 0) TRACE(41);
+            if (threadIdx.x == 64) TRACE(41);
         }
     }
 
@@ -660,7 +673,7 @@ cudaError_t launch_tc(const CUtensorMap& mq, const CUtensorMap& mkv, const TcPar
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(mla_decode_tc_kernel<NPAD>),
                                       C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return launch_pdl(mla_decode_tc_kernel<NPAD>, dim3(grid), dim3(kThreads), size_t(C::kSmemBytes),
+    return launch_pdl(mla_decode_tc_kernel<NPAD>, dim3(grid), dim3(C::kThreads), size_t(C::kSmemBytes),
                       stream, mq, mkv, prm);
 }
 
