@@ -293,12 +293,14 @@ class Step:
                                   out, lse, self.ws, self.w.scale)
 
     def run(self, q=None, bt=None, ctx=None, decode_events=None, row_events=None):
-        for i, c in enumerate(self.calls):
-            if decode_events is not None:
-                decode_events[i][0].record()
+        """One step.  decode_events: a (start, end) pair recorded around the step's
+        back-to-back decode calls; row_events: pairs around the merge and the migration."""
+        if decode_events is not None:
+            decode_events[0].record()
+        for c in self.calls:
             self.decode(c, q, bt, ctx)
-            if decode_events is not None:
-                decode_events[i][1].record()
+        if decode_events is not None:
+            decode_events[1].record()
         if self.merge:
             if row_events is not None:
                 row_events["lse_merge"][0].record()
@@ -346,8 +348,12 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     K, Wm = args.steps, args.warmup
 
-    # one eager pass (caches the per-device state), then one CUDA graph per timed step
-    # with in-graph events around every decode call
+    # one eager pass (caches the per-device state), then two sets of CUDA graphs of one
+    # step each: plain graphs for the headline timing, and instrumented graphs with
+    # in-graph events around the decode calls, the merge and the migration for the
+    # per-row breakdown.  Event nodes inside a graph end the programmatic-dependent-
+    # launch overlap between neighbouring kernels and add latency, so they stay out of
+    # the headline graphs.
     step.run()
     torch.cuda.synchronize()
 
@@ -357,17 +363,22 @@ def run_ours(args, world, rank, local):
         except TypeError:
             return None
 
-    graphs, dec_ev, row_ev = [], [], []
     side = torch.cuda.Stream(device)
-    for k in range(max(K, 1)):
-        evs = [(new_event(), new_event()) for _ in step.calls]
-        rows = {n: (new_event(), new_event()) for n in ("lse_merge", "kv_migrate")}
-        if any(e is None for pair in evs for e in pair):
-            evs, rows = None, None
+
+    def capture(**kw):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=side):
-            step.run(decode_events=evs, row_events=rows)
-        graphs.append(g)
+            step.run(**kw)
+        return g
+
+    graphs = [capture() for _ in range(max(K, 1))]
+    inst, dec_ev, row_ev = [], [], []
+    for k in range(max(K, 1)):
+        evs = (new_event(), new_event())
+        rows = {n: (new_event(), new_event()) for n in ("lse_merge", "kv_migrate")}
+        if None in evs or any(e is None for pair in rows.values() for e in pair):
+            break
+        inst.append(capture(decode_events=evs, row_events=rows))
         dec_ev.append(evs)
         row_ev.append(rows)
     stream = torch.cuda.current_stream(device)
@@ -376,6 +387,7 @@ def run_ours(args, world, rank, local):
         graphs[k % len(graphs)].replay()
     torch.cuda.synchronize()
 
+    # timed region: K plain steps, the L2 flushed before each
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
@@ -388,10 +400,20 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
     barrier(world)
     step_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    if dec_ev[0] is not None:
-        dec_ms = [a.elapsed_time(b) for k in range(K) for a, b in dec_ev[k]]
-        dec_src = "CUDA events captured inside the step graph around each decode call"
+
+    # breakdown: K instrumented steps, same flush
+    ncalls = len(step.calls)
+    if len(inst) == max(K, 1):
+        for k in range(K):
+            flush.zero_()
+            inst[k].replay()
+        torch.cuda.synchronize()
+        dec_ms = [dec_ev[k][0].elapsed_time(dec_ev[k][1]) / ncalls for k in range(K)]
+        dec_src = (f"CUDA events captured inside instrumented step graphs around the step's "
+                   f"{ncalls} back-to-back decode call(s) (a second timed pass of K steps); "
+                   f"per call = their span / {ncalls}")
     else:   # events cannot be captured: time graph replays of single decode calls
+        row_ev = [None]
         dec_ms = []
         for c in step.calls[:2]:
             g1 = torch.cuda.CUDAGraph()

@@ -39,11 +39,25 @@ constexpr int kSoftmaxBarrier = 1;             // named barrier id of the first 
 constexpr int kColBlockBytes = kTileTokens * 128;  // one 64-column block of a tile: 16 KB
 constexpr int kPairBytes = 2 * kColBlockBytes;
 constexpr float kTau = 8.0f;                   // rescale only when a score beats the max by 2^8
+// One warp's TMA issue stream moves ~40 GB/s into an SM; the loads are spread over
+// kProducerWarps warps so that one SM can ingest a tile at ~3x that rate.
+constexpr int kProducerWarps = 3;
+#ifndef SPLASH_TRACE_TILE0
+#define SPLASH_TRACE_TILE0 0
+#endif
+constexpr int kTraceTile0 = SPLASH_TRACE_TILE0;  // first tile of a piece the trace stamps
+
+// Whether producer warp pw issues any of the boxes g0 .. g0 + n - 1 (box b belongs to
+// warp b % kProducerWarps).
+__device__ __forceinline__ bool owns_box(int g0, int n, int pw) {
+    return n >= kProducerWarps || (pw - g0 % kProducerWarps + kProducerWarps) % kProducerWarps < n;
+}
 
 template <int NPAD>
 struct TcConfig {
     static constexpr int kSoftmaxGroups = NPAD == 64 ? 2 : 1;  // warpgroups sharing the heads
-    static constexpr int kThreads = 64 + 128 * kSoftmaxGroups;
+    static constexpr int kFirstExtraProducer = 2 + 4 * kSoftmaxGroups;  // warps after the softmax
+    static constexpr int kThreads = 32 * (kFirstExtraProducer + kProducerWarps - 1);
     static constexpr int kPairs = NPAD == 64 ? 4 : 5;      // pair slots (ring)
     static constexpr int kRopes = NPAD == 16 ? 2 : 1;      // rope / P^T slots (ring)
     static constexpr int kQBytes = 9 * NPAD * 128;
@@ -260,9 +274,12 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
     const int64_t aj = (T > 0 && j < G) ? group_start(j, T, G) : 0;
     const int64_t bj = (T > 0 && j < G) ? group_start(j + 1, T, G) : 0;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        // The whole warp walks the schedule (so it stays converged); lane 0 issues.
+    if (warp == 0 || warp >= C::kFirstExtraProducer) {
+        // ------------------------------------------------------------ TMA producers
+        // kProducerWarps warps walk the same schedule (each whole warp, so it stays
+        // converged); load slot k of a tile (pairs 0-3, then the rope block) and Q box k
+        // belong to producer warp k % kProducerWarps, whose lanes issue them.
+        const int pw = warp == 0 ? 0 : warp - C::kFirstExtraProducer + 1;
         if (aj < bj) {
             const uint64_t pol_kv = policy_evict_first();
             const uint64_t pol_q = policy_evict_last();
@@ -275,14 +292,14 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                 if (!warp_wait(q_empty, qph ^ 1, abort_flag, status)) { ok = false; break; }
                 qph ^= 1;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(q_full, C::kQBytes);
+                    if (pw == 0) mbar_arrive_expect_tx(q_full, C::kQBytes);
                     const int qrow = pc.r * a.H + a.head_lo + hbase;
-                    for (int cb = 0; cb < 9; ++cb)
+                    for (int cb = pw; cb < 9; cb += kProducerWarps)
                         tma_load_2d(sQ + cb * NPAD * 128, &map_q, q_full, cb * 64, qrow, pol_q);
-                    TRACE(3);
+                    if (pw == 0) TRACE(3);
                 }
                 __syncwarp();
-                int ttr = 0;
+                int ttr = -kTraceTile0;
                 const int32_t* bt = a.block_table + int64_t(pc.r) * a.max_pages;
                 for (int t = pc.t_lo; t < pc.t_hi && ok; ++t) {
                     const int tok0 = (p.tile0 + t) * kTileTokens;
@@ -298,32 +315,49 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                         }
                     }
                     const uint32_t present = __ballot_sync(0xffffffffu, my_pid >= 0);
-                    if (__any_sync(0xffffffffu, bad) && lane == 0)
+                    if (pw == 0 && __any_sync(0xffffffffu, bad) && lane == 0)
                         atomicOr(status, uint32_t(SPLASH_DEVICE_BAD_INPUT));
                     const uint32_t blk_bytes = uint32_t(__popc(present)) * P * 128;
-                    if (lane == 0 && ttr < 3) TRACE(4 + ttr * 3);
+                    if (pw == 0 && lane == 0 && unsigned(ttr) < 3u) TRACE(4 + ttr * 3);
+                    // box b of the tile (pair jj, page k, column block c2: b = jj * bpp + 2k + c2;
+                    // rope block of page k: b = 4 * bpp + k) is issued by producer warp
+                    // b % kProducerWarps, so the boxes that wait for the last PV of the
+                    // previous tile (pair 3 and the rope) spread over all producer warps
+                    const int bpp = 2 * pages_per_tile;  // boxes per pair
                     for (int jj = 0; jj < 4; ++jj) {
-                        if (!warp_wait(&pair_empty[ps], pph ^ 1, abort_flag, status)) { ok = false; break; }
-                        if (lane == 0) mbar_arrive_expect_tx(&pair_full[ps], 2 * blk_bytes);
-                        __syncwarp();
-                        uint8_t* slot = sPair + ps * kPairBytes;
-                        if (my_pid >= 0)
-                            for (int c2 = 0; c2 < 2; ++c2)
-                                tma_load_2d(slot + c2 * kColBlockBytes + lane * P * 128, &map_kv,
-                                            &pair_full[ps], (2 * jj + c2) * 64, my_pid * P, pol_kv);
-                        __syncwarp();
+                        const int g0 = jj * bpp;
+                        if (owns_box(g0, bpp, pw)) {
+                            if (!warp_wait(&pair_empty[ps], pph ^ 1, abort_flag, status)) { ok = false; break; }
+                            if (lane == 0 && g0 % kProducerWarps == pw) {
+                                mbar_arrive_expect_tx(&pair_full[ps], 2 * blk_bytes);
+                                if (ttr == 1) TRACE(55 + jj);
+                            }
+                            __syncwarp();
+                            uint8_t* slot = sPair + ps * kPairBytes;
+                            if (my_pid >= 0)
+                                for (int c2 = 0; c2 < 2; ++c2)
+                                    if ((g0 + 2 * lane + c2) % kProducerWarps == pw)
+                                        tma_load_2d(slot + c2 * kColBlockBytes + lane * P * 128, &map_kv,
+                                                    &pair_full[ps], (2 * jj + c2) * 64, my_pid * P, pol_kv);
+                            __syncwarp();
+                        }
                         if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
                     }
                     if (!ok) break;
-                    if (lane == 0 && ttr < 3) TRACE(5 + ttr * 3);
-                    if (!warp_wait(&rope_empty[rs], rph ^ 1, abort_flag, status)) { ok = false; break; }
-                    if (lane == 0) mbar_arrive_expect_tx(&rope_full[rs], blk_bytes);
-                    __syncwarp();
-                    if (my_pid >= 0)
-                        tma_load_2d(sRope + rs * kColBlockBytes + lane * P * 128, &map_kv,
-                                    &rope_full[rs], 8 * 64, my_pid * P, pol_kv);
-                    __syncwarp();
-                    if (lane == 0 && ttr < 3) TRACE(6 + ttr * 3);
+                    if (pw == 0 && lane == 0 && unsigned(ttr) < 3u) TRACE(5 + ttr * 3);
+                    const int g0 = 4 * bpp;
+                    if (owns_box(g0, pages_per_tile, pw)) {
+                        if (!warp_wait(&rope_empty[rs], rph ^ 1, abort_flag, status)) { ok = false; break; }
+                        if (lane == 0 && g0 % kProducerWarps == pw)
+                            mbar_arrive_expect_tx(&rope_full[rs], blk_bytes);
+                        __syncwarp();
+                        if (my_pid >= 0 && (g0 + lane) % kProducerWarps == pw)
+                            tma_load_2d(sRope + rs * kColBlockBytes + lane * P * 128, &map_kv,
+                                        &rope_full[rs], 8 * 64, my_pid * P, pol_kv);
+                        __syncwarp();
+                        if (pw == g0 % kProducerWarps && lane == 0 && unsigned(ttr) < 3u)
+                            TRACE(6 + ttr * 3);
+                    }
                     ++ttr;
                     if (++rs == C::kRopes) { rs = 0; rph ^= 1; }
                 }
@@ -353,14 +387,15 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
             while (ok && it.next(pc, p)) {
                 if (!warp_wait(q_full, qph, abort_flag, status)) { ok = false; break; }
                 qph ^= 1;
-                int ttr = 0;
+                int ttr = -kTraceTile0;
                 for (int t = pc.t_lo; t < pc.t_hi; ++t) {
                     const bool first = (t == pc.t_lo), last = (t + 1 == pc.t_hi);
                     const int ps0 = ps;
-                    if (lane == 0 && ttr < 3) TRACE(13 + ttr * 5);
+                    if (lane == 0 && unsigned(ttr) < 3u) TRACE(13 + ttr * 5);
                     // S^T = K_tile . Q^T over the 512 latent dims (pairs) ...
                     for (int jj = 0; jj < 4; ++jj) {
                         if (!warp_wait(&pair_full[ps], pph, abort_flag, status)) { ok = false; break; }
+                        if (lane == 0 && ttr == 1) TRACE(51 + jj);
                         tc_fence_after();
                         if (lane == 0) {
                             const uint64_t da_s = dk0 + uint64_t(ps) * (kPairBytes >> 4);
@@ -379,7 +414,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                     if (!ok) break;
                     // ... and the 64 rope dims
                     if (!warp_wait(&rope_full[rs], rph, abort_flag, status)) { ok = false; break; }
-                    if (lane == 0 && ttr < 3) TRACE(14 + ttr * 5);
+                    if (lane == 0 && unsigned(ttr) < 3u) TRACE(14 + ttr * 5);
                     tc_fence_after();
                     if (lane == 0) {
                         const uint64_t da_r = dr0 + uint64_t(rs) * (kColBlockBytes >> 4);
@@ -389,13 +424,13 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                                         dq0 + ((8 * NPAD * 128 + k4 * 32) >> 4), idesc_qk, 1u);
                         tc_commit(s_full);
                         if (last) tc_commit(q_empty);
-                        if (ttr < 3) TRACE(15 + ttr * 5);
+                        if (unsigned(ttr) < 3u) TRACE(15 + ttr * 5);
                     }
                     __syncwarp();
                     // O^T += V^T . P^T once the softmax has written P^T into the rope slot
                     if (!warp_wait(p_full, pfph, abort_flag, status)) { ok = false; break; }
                     pfph ^= 1;
-                    if (lane == 0 && ttr < 3) TRACE(16 + ttr * 5);
+                    if (lane == 0 && unsigned(ttr) < 3u) TRACE(16 + ttr * 5);
                     if (first) {
                         if (!warp_wait(o_free, ofph ^ 1, abort_flag, status)) { ok = false; break; }
                         ofph ^= 1;
@@ -413,16 +448,17 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                                 mma_bf16_ss(o_tmem + jj * NPAD, da_v + ((kk * 2048) >> 4),
                                             db_p + ((kk * 2048) >> 4), idesc_pv,
                                             (!first || kk > 0) ? 1u : 0u);
-                                if (jj == 0 && kk == 0 && ttr < 2) TRACE(43 + ttr * 4);
+                                if (jj == 0 && kk == 0 && unsigned(ttr) < 2u) TRACE(43 + ttr * 4);
                             }
                             tc_commit(&pair_empty[pslot]);
-                            if (jj == 0 && ttr < 2) TRACE(44 + ttr * 4);
-                            if (jj == 1 && ttr < 2) TRACE(45 + ttr * 4);
-                            if (jj == 2 && ttr < 2) TRACE(46 + ttr * 4);
+                            if (jj == 0 && unsigned(ttr) < 2u) TRACE(44 + ttr * 4);
+                            if (jj == 1 && unsigned(ttr) < 2u) TRACE(45 + ttr * 4);
+                            if (jj == 2 && unsigned(ttr) < 2u) TRACE(46 + ttr * 4);
+
                         }
                         tc_commit(&rope_empty[rs]);
                         if (last) tc_commit(o_full);
-                        if (ttr < 3) TRACE(17 + ttr * 5);
+                        if (unsigned(ttr) < 3u) TRACE(17 + ttr * 5);
                     }
                     __syncwarp();
                     ++ttr;
@@ -480,8 +516,8 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                 if (named_barrier_or(bar, kSoftmaxThreads, !w)) { ok = false; break; }
                 sph ^= 1;
                 tc_fence_after();
-                const int ttr = t - pc.t_lo;
-                if (threadIdx.x == 64 && ttr < 3) TRACE(28 + ttr * 4);
+                const int ttr = t - pc.t_lo - kTraceTile0;
+                if (threadIdx.x == 64 && unsigned(ttr) < 3u) TRACE(28 + ttr * 4);
                 // pass 1: does any valid score exceed the running max by more than tau?
                 float excess = -INFINITY;
 #pragma unroll
@@ -495,7 +531,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                 }
                 if (!valid) excess = -INFINITY;
                 const bool rescale = named_barrier_or(bar, kSoftmaxThreads, excess > kTau);
-                if (threadIdx.x == 64 && ttr < 3) TRACE(29 + ttr * 4);
+                if (threadIdx.x == 64 && unsigned(ttr) < 3u) TRACE(29 + ttr * 4);
                 if (rescale) {
                     // exact column max over the tile's valid tokens: warp reduce-scatter in
                     // chunks of up to 32 heads, then the 4 warps through shared memory
@@ -547,7 +583,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                     if (st < HW) sm_m[hw0 + st] = sm_mnew[hw0 + st];
                     named_barrier_sync(bar, kSoftmaxThreads);
                 }
-                if (threadIdx.x == 64 && ttr < 3) TRACE(30 + ttr * 4);
+                if (threadIdx.x == 64 && unsigned(ttr) < 3u) TRACE(30 + ttr * 4);
                 // pass 2: P^T row = exp2(s * c - m) as bf16 into the rope slot (MN-major,
                 // 128-byte swizzle: 16-byte chunk ch of row r sits at chunk ch ^ (r & 7))
                 uint8_t* prow = sRope + rs * kColBlockBytes + row * 128;
@@ -589,7 +625,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(p_full);
-                if (threadIdx.x == 64 && ttr < 3) TRACE(31 + ttr * 4);
+                if (threadIdx.x == 64 && unsigned(ttr) < 3u) TRACE(31 + ttr * 4);
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
@@ -630,22 +666,23 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                 lbase = plse + slot * a.Hs + hbase;
             }
             hstride = kDv;
+            // per 16 heads: the four dv blocks' loads are in flight together, then stored
 #pragma unroll 1
             for (int c = 0; c < HW / 16; ++c) {
                 const int hc = hw0 + c * 16;
+                float o[4][16];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) tmem_ld16(o_tmem + jj * NPAD + hc, o[jj]);
                 float inv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) inv[e] = sm_alpha[hc + e];
                 float* ocol = obase + int64_t(hc) * hstride + row;
-#pragma unroll 1
-                for (int jj = 0; jj < 4; ++jj) {
-                    float o[16];
-                    tmem_ld16(o_tmem + jj * NPAD + hc, o);
-                    tmem_wait_ld();
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        if (hc + e < nh) ocol[e * hstride + jj * 128] = o[e] * inv[e];
-                }
+                        if (hc + e < nh) ocol[e * hstride + jj * 128] = o[jj][e] * inv[e];
             }
             if (st < HW && hw0 + st < nh) {
                 const int h = hw0 + st;

@@ -23,6 +23,19 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
+// Optional kernel-boundary trace (compiled in only with -DSPLASH_TRACE): globaltimer
+// stamps of the plan and combine kernels, read back with splash_ktrace_read().
+#ifdef SPLASH_TRACE
+__device__ unsigned long long g_ktrace[8];
+#define KTRACE_SET(slot) (g_ktrace[slot] = globaltimer_ns())
+#define KTRACE_MIN(slot) atomicMin(&g_ktrace[slot], globaltimer_ns())
+#define KTRACE_MAX(slot) atomicMax(&g_ktrace[slot], globaltimer_ns())
+#else
+#define KTRACE_SET(slot) ((void)0)
+#define KTRACE_MIN(slot) ((void)0)
+#define KTRACE_MAX(slot) ((void)0)
+#endif
+
 // Inclusive block scan of one int64 per thread (kPlanThreads threads).
 __device__ int64_t block_inclusive_scan(int64_t v, int64_t* warp_sums) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -48,55 +61,71 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* warp_sums) {
     return v + add;
 }
 
+// Clipped token range and tile span of one request (the plan's per-request part
+// that depends on nothing but its context length).
+__device__ __forceinline__ ReqPlan request_span(int L, int64_t tok_lo, int64_t tok_hi) {
+    const int64_t lo = tok_lo;
+    const int64_t hi = tok_hi < 0 ? int64_t(L) : min(tok_hi, int64_t(L));
+    ReqPlan p;
+    p.ctx_len = L;
+    if (hi <= lo) {
+        p.lo = p.hi = 0;
+        p.tile0 = 0;
+        p.ntiles = 0;
+    } else {
+        p.lo = int32_t(lo);
+        p.hi = int32_t(hi);
+        p.tile0 = int32_t(lo / kTileTokens);
+        p.ntiles = int32_t((hi + kTileTokens - 1) / kTileTokens - lo / kTileTokens);
+    }
+    p.tile_begin = 0;
+    p.first_grp = 0;
+    p.nsplit = 0;
+    p.slot_base = -1;
+    p.pad[0] = p.pad[1] = 0;
+    return p;
+}
+
+// Requests whose tile ends the plan keeps in shared memory for the group search;
+// larger batches search the plan in global memory.
+constexpr int kPlanSmemReqs = 8192;
+
+// One CTA.  Every thread owns a contiguous run of requests; the run is recomputed
+// from ctx_lens in each pass (an L1 hit after the first) so that nothing written to
+// global memory is read back, and the group search runs over shared memory.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ ctx_lens,
                                                             int B, int64_t tok_lo, int64_t tok_hi,
                                                             int max_ctx, int num_groups, int Hs,
                                                             uint8_t* __restrict__ ws) {
+    extern __shared__ int64_t s_end[];  // [B] tile ends, when B <= kPlanSmemReqs
     __shared__ int64_t warp_sums[32];
     __shared__ int64_t s_total;
+    if (threadIdx.x == 0) KTRACE_SET(0);
     pdl_wait();
     pdl_trigger();  // the decode grid may start its prologue now
+    if (threadIdx.x == 0) KTRACE_SET(1);
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
     const WorkspaceLayout lay(B, Hs, num_groups);
     ReqPlan* req = reinterpret_cast<ReqPlan*>(ws + lay.req_off);
+    const bool smem_ends = B <= kPlanSmemReqs;
 
     const int per = (B + kPlanThreads - 1) / kPlanThreads;
-    const int r0 = threadIdx.x * per;
+    const int r0 = min(B, int(threadIdx.x) * per);
     const int r1 = min(B, r0 + per);
-    bool bad = false;
-
-    // Pass 1: clipped ranges and tile counts.
-    int64_t my_tiles = 0;
-    for (int r = r0; r < r1; ++r) {
+    auto clipped_len = [&](int r, bool& bad) {
         int L = ctx_lens[r];
         if (L < 0 || L > max_ctx) {
             bad = true;
             L = min(max(L, 0), max_ctx);
         }
-        int64_t lo = tok_lo;
-        int64_t hi = tok_hi < 0 ? int64_t(L) : min(tok_hi, int64_t(L));
-        ReqPlan p;
-        p.ctx_len = L;
-        if (hi <= lo) {
-            p.lo = p.hi = 0;
-            p.tile0 = 0;
-            p.ntiles = 0;
-        } else {
-            p.lo = int32_t(lo);
-            p.hi = int32_t(hi);
-            p.tile0 = int32_t(lo / kTileTokens);
-            p.ntiles = int32_t((hi + kTileTokens - 1) / kTileTokens - lo / kTileTokens);
-        }
-        p.tile_begin = my_tiles;  // thread-local prefix for now
-        p.first_grp = 0;
-        p.nsplit = 0;
-        p.slot_base = -1;
-        p.pad[0] = p.pad[1] = 0;
-        req[r] = p;
-        my_tiles += p.ntiles;
-    }
+        return L;
+    };
+
+    // Pass 1: tile counts.
+    bool bad = false;
+    int64_t my_tiles = 0;
+    for (int r = r0; r < r1; ++r) my_tiles += request_span(clipped_len(r, bad), tok_lo, tok_hi).ntiles;
     const int64_t incl = block_inclusive_scan(my_tiles, warp_sums);
-    const int64_t excl = incl - my_tiles;
     if (threadIdx.x == kPlanThreads - 1) s_total = incl;
     __syncthreads();
     const int64_t T = s_total;
@@ -106,27 +135,43 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 
     // Pass 2: global tile offsets, CTA-group cut and partial-slot counts.
     int64_t my_slots = 0;
-    for (int r = r0; r < r1; ++r) {
-        ReqPlan& p = req[r];
-        p.tile_begin += excl;
-        if (p.ntiles > 0) {
-            const int64_t g0 = group_of_tile(p.tile_begin, T, G);
-            const int64_t g1 = group_of_tile(p.tile_begin + p.ntiles - 1, T, G);
-            p.first_grp = int32_t(g0);
-            p.nsplit = int32_t(g1 - g0 + 1);
-            if (p.nsplit > 1) my_slots += p.nsplit;
+    {
+        int64_t tb = incl - my_tiles;
+        bool unused = false;
+        for (int r = r0; r < r1; ++r) {
+            const ReqPlan p = request_span(clipped_len(r, unused), tok_lo, tok_hi);
+            if (p.ntiles > 0) {
+                const int64_t nsplit = group_of_tile(tb + p.ntiles - 1, T, G) - group_of_tile(tb, T, G) + 1;
+                if (nsplit > 1) my_slots += nsplit;
+            }
+            tb += p.ntiles;
         }
     }
     const int64_t sincl = block_inclusive_scan(my_slots, warp_sums);
-    int64_t slot = sincl - my_slots;
-    for (int r = r0; r < r1; ++r) {
-        ReqPlan& p = req[r];
-        if (p.nsplit > 1) {
-            p.slot_base = int32_t(slot);
-            slot += p.nsplit;
+
+    // Pass 3: the complete request plans.
+    {
+        int64_t tb = incl - my_tiles, slot = sincl - my_slots;
+        bool unused = false;
+        for (int r = r0; r < r1; ++r) {
+            ReqPlan p = request_span(clipped_len(r, unused), tok_lo, tok_hi);
+            p.tile_begin = tb;
+            if (p.ntiles > 0) {
+                const int64_t g0 = group_of_tile(tb, T, G);
+                const int64_t g1 = group_of_tile(tb + p.ntiles - 1, T, G);
+                p.first_grp = int32_t(g0);
+                p.nsplit = int32_t(g1 - g0 + 1);
+                if (p.nsplit > 1) {
+                    p.slot_base = int32_t(slot);
+                    slot += p.nsplit;
+                }
+            }
+            req[r] = p;
+            tb += p.ntiles;
+            if (smem_ends) s_end[r] = tb;
         }
     }
-    const bool any_bad = __syncthreads_or(bad);   // also orders the tile_begin updates
+    const bool any_bad = __syncthreads_or(bad);  // also publishes s_end
     // First request of every CTA group: smallest r whose tiles reach past the group start,
     // so a decode CTA finds its first piece with one load instead of a search.
     int32_t* first_req = reinterpret_cast<int32_t*>(ws + lay.grp_off);
@@ -135,7 +180,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         int lo = 0, hi = B;
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
-            if (req[mid].tile_begin + req[mid].ntiles > x) hi = mid;
+            const int64_t end = smem_ends ? s_end[mid] : req[mid].tile_begin + req[mid].ntiles;
+            if (end > x) hi = mid;
             else lo = mid + 1;
         }
         first_req[j] = lo;
@@ -148,6 +194,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         hdr->heads = Hs;
         hdr->max_slots = lay.max_slots;
         hdr->slots_used = int32_t(sincl);
+        KTRACE_SET(2);
     }
 }
 
@@ -218,8 +265,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict_
                                                       int head_lo, int Hs, int num_groups,
                                                       float* __restrict__ out,
                                                       float* __restrict__ lse) {
+    if (threadIdx.x == 0) KTRACE_MIN(3);
     pdl_wait();
     pdl_trigger();
+    if (threadIdx.x == 0) KTRACE_MIN(4);
+    if (threadIdx.x == 0) KTRACE_MAX(5);
     const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (row >= int64_t(B) * Hs) return;
     const int r = int(row / Hs), hh = int(row % Hs);
@@ -258,10 +308,25 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
 
 }  // namespace
 
+#ifdef SPLASH_TRACE
+extern "C" __attribute__((visibility("default"))) int splash_ktrace_read(void* host_dst) {
+    return cudaMemcpyFromSymbol(host_dst, g_ktrace, sizeof(g_ktrace)) == cudaSuccess ? 0 : -1;
+}
+extern "C" __attribute__((visibility("default"))) int splash_ktrace_clear() {
+    const unsigned long long init[8] = {0, 0, 0, ~0ull, ~0ull, 0, 0, 0};
+    return cudaMemcpyToSymbol(g_ktrace, init, sizeof(init)) == cudaSuccess ? 0 : -1;
+}
+#endif
+
 cudaError_t launch_plan(const int32_t* ctx_lens, int B, int64_t tok_lo, int64_t tok_hi, int max_ctx,
                         int num_groups, int Hs, void* ws, cudaStream_t stream) {
-    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, ctx_lens, B, tok_lo,
-                      tok_hi, max_ctx, num_groups, Hs, static_cast<uint8_t*>(ws));
+    const int smem = B <= kPlanSmemReqs ? B * int(sizeof(int64_t)) : 0;
+    if (smem > 48 * 1024) {
+        cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(plan_kernel), smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), size_t(smem), stream, ctx_lens, B,
+                      tok_lo, tok_hi, max_ctx, num_groups, Hs, static_cast<uint8_t*>(ws));
 }
 
 cudaError_t launch_combine(const void* ws, int B, int H, int head_lo, int Hs, int num_groups,
