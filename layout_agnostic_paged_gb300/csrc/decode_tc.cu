@@ -518,17 +518,18 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                 tc_fence_after();
                 const int ttr = t - pc.t_lo - kTraceTile0;
                 if (threadIdx.x == 64 && unsigned(ttr) < 3u) TRACE(28 + ttr * 4);
+                // the tile's scores of this thread's token for the group's heads, read once
+                float sv[HW / 16][16];
+#pragma unroll
+                for (int c = 0; c < HW / 16; ++c) tmem_ld16(s_tmem + hw0 + c * 16, sv[c]);
+                tmem_wait_ld();
                 // pass 1: does any valid score exceed the running max by more than tau?
                 float excess = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < HW / 16; ++c) {
-                    float s[16];
-                    tmem_ld16(s_tmem + hw0 + c * 16, s);
-                    tmem_wait_ld();
+                for (int c = 0; c < HW / 16; ++c)
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        excess = fmaxf(excess, s[e] * cl - sm_m[hw0 + c * 16 + e]);
-                }
+                        excess = fmaxf(excess, sv[c][e] * cl - sm_m[hw0 + c * 16 + e]);
                 if (!valid) excess = -INFINITY;
                 const bool rescale = named_barrier_or(bar, kSoftmaxThreads, excess > kTau);
                 if (threadIdx.x == 64 && unsigned(ttr) < 3u) TRACE(29 + ttr * 4);
@@ -536,18 +537,14 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                     // exact column max over the tile's valid tokens: warp reduce-scatter in
                     // chunks of up to 32 heads, then the 4 warps through shared memory
                     constexpr int RS = HW < 32 ? HW : 32;
-#pragma unroll 1
-                    for (int h0 = hw0; h0 < hw0 + HW; h0 += RS) {
+#pragma unroll
+                    for (int i0 = 0; i0 < HW; i0 += RS) {
                         float v[RS];
 #pragma unroll
-                        for (int c = 0; c < RS / 16; ++c) {
-                            float s[16];
-                            tmem_ld16(s_tmem + h0 + c * 16, s);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) v[c * 16 + e] = valid ? s[e] * cl : -INFINITY;
-                        }
+                        for (int i = 0; i < RS; ++i)
+                            v[i] = valid ? sv[(i0 + i) / 16][(i0 + i) % 16] * cl : -INFINITY;
                         const float m = warp_reduce_scatter<RS, true>(v, lane);
+                        const int h0 = hw0 + i0;
                         if (RS == 32) sm_red[quad * NPAD + h0 + lane] = m;
                         else if ((lane & 1) == 0) sm_red[quad * NPAD + h0 + (lane >> 1)] = m;
                     }
@@ -589,14 +586,11 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                 uint8_t* prow = sRope + rs * kColBlockBytes + row * 128;
 #pragma unroll
                 for (int c = 0; c < HW / 16; ++c) {
-                    float s[16];
-                    tmem_ld16(s_tmem + hw0 + c * 16, s);
-                    tmem_wait_ld();
                     uint32_t pk[8];
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
-                        float p0 = valid ? ex2_approx(s[e] * cl - sm_m[hw0 + c * 16 + e]) : 0.f;
-                        float p1 = valid ? ex2_approx(s[e + 1] * cl - sm_m[hw0 + c * 16 + e + 1]) : 0.f;
+                        float p0 = valid ? ex2_approx(sv[c][e] * cl - sm_m[hw0 + c * 16 + e]) : 0.f;
+                        float p1 = valid ? ex2_approx(sv[c][e + 1] * cl - sm_m[hw0 + c * 16 + e + 1]) : 0.f;
                         pk[e / 2] = pack_bf16x2(p0, p1);
                         lpart[c * 16 + e] += p0;       // l from the unrounded fp32 P
                         lpart[c * 16 + e + 1] += p1;

@@ -200,15 +200,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 
 // Merge `S` partial rows (out at stride `ostride` floats, lse at stride `lstride`)
 // into one output row; one warp.  Lane s < 32 owns split s's weight (broadcast by
-// shuffles); lanes cover d_v in float4 steps with up to 4 independent loads per
-// split in flight per lane.
+// shuffles, the lse column read once); lanes cover d_v in float4 steps with the
+// loads of up to 4 splits (16 float4 per lane) in flight.
 __device__ __forceinline__ void warp_lse_merge(const float* __restrict__ pout, int64_t ostride,
                                                const float* __restrict__ plse, int64_t lstride,
                                                int S, int d_v, float* __restrict__ out,
                                                float* __restrict__ lse) {
     const int lane = threadIdx.x & 31;
-    float m = -INFINITY;
-    for (int s0 = 0; s0 < S; s0 += 32)
+    // up to 32 splits: one load of the lse column, kept in a register for all passes
+    const float l0 = (lane < S) ? plse[lane * lstride] : -INFINITY;
+    float m = l0;
+    for (int s0 = 32; s0 < S; s0 += 32)
         if (s0 + lane < S) m = fmaxf(m, plse[(s0 + lane) * lstride]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -218,8 +220,8 @@ __device__ __forceinline__ void warp_lse_merge(const float* __restrict__ pout, i
         if (lane == 0) *lse = -INFINITY;
         return;
     }
-    float wsum = 0.f;
-    for (int s0 = 0; s0 < S; s0 += 32)
+    float wsum = (lane < S) ? expf(l0 - m) : 0.f;
+    for (int s0 = 32; s0 < S; s0 += 32)
         if (s0 + lane < S) wsum += expf(plse[(s0 + lane) * lstride] - m);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
@@ -229,9 +231,10 @@ __device__ __forceinline__ void warp_lse_merge(const float* __restrict__ pout, i
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s0 = 0; s0 < S; s0 += 32) {
-            const float myw = (s0 + lane < S) ? expf(plse[(s0 + lane) * lstride] - m) : 0.f;
+            const float myw = s0 == 0 ? ((lane < S) ? expf(l0 - m) : 0.f)
+                                      : ((s0 + lane < S) ? expf(plse[(s0 + lane) * lstride] - m) : 0.f);
             const int n = min(32, S - s0);
-#pragma unroll 2
+#pragma unroll 4
             for (int t = 0; t < n; ++t) {
                 const float w = __shfl_sync(0xffffffffu, myw, t);
                 const float* src = pout + (s0 + t) * ostride + j0 + lane * 4;
