@@ -533,7 +533,7 @@ def cpu_baseline(w, inp, seconds: float):
     # grow the sample (requests, cycling) until it takes about `seconds`
     t_total, toks, n = 0.0, 0, 0
     r = 0
-    while t_total < seconds and n < 10 * B:
+    while t_total < seconds and n < 1000 * B:
         t0 = time.perf_counter()
         oracle.decode_attn(q[r:r + 1], pool, bt[r:r + 1], ctx[r:r + 1], w.scale)
         t_total += time.perf_counter() - t0
