@@ -15,15 +15,18 @@
 // O^T (4N columns) fit in the 512 TMEM columns of one SM.  V is the latent
 // prefix of the key: the same shared-memory tile feeds both contractions.
 //
-// Roles (one CTA per SM, persistent over the split plan's pieces; 192 threads, or
-// 320 at N = 64 where two softmax warpgroups each own half of the heads):
-//   warp 0      TMA producer: Q of the piece, then per tile four 32 KB "pairs"
-//               (latent column blocks 2j, 2j+1) and the 16 KB rope block, each page
-//               fetched through the block table (2D tiled loads, 128-byte swizzle)
+// Roles (one CTA per SM, persistent over the split plan's pieces; 256 threads, or
+// 384 at N = 64 where two softmax warpgroups each own half of the heads):
+//   warp 0 and  TMA producers: Q of the piece, then per tile four 32 KB "pairs"
+//   the last    (latent column blocks 2j, 2j+1) and the 16 KB rope block, each page
+//   two warps   fetched through the block table (2D tiled loads, 128-byte swizzle);
+//               the boxes are dealt round-robin to the three warps
 //   warp 1      TMEM allocation and the single MMA-issuing thread
 //   warps 2-5   softmax (S^T from TMEM -> P^T bf16 into the rope slot), zeroing of
 //   (6-9)       V rows past the context (poisoned tails never reach the tensor
 //               core), O rescale, and the epilogue (O^T / l -> out or a partial)
+// At N = 64, Q and one tile fill shared memory, so a tile's last pair and its rope
+// block are fetched only after the previous tile's PV has released their slots.
 // Every wait is bounded (see common.cuh); a timeout sets the workspace status
 // bit and the CTA unwinds.
 #include <math.h>
