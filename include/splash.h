@@ -134,6 +134,48 @@ SPLASH_API int splash_decode_attn(const splash_attn_desc* desc, const void* q, c
                        void* workspace, size_t ws_bytes, splash_stream_t stream);
 
 /*
+ * Per-request token ranges and storage rows for splash_decode_attn_ex.  Every
+ * pointer may be NULL, and NULL restores the splash_decode_attn behaviour for
+ * that field.
+ *   tok_lo, tok_hi  int32 [B] device: request r's token set is
+ *                   [tok_lo[r], min(tok_hi[r] < 0 ? ctx_len : tok_hi[r], ctx_len)),
+ *                   for CP with an uneven share per request (the "ideal token
+ *                   partitioning" of Appendix, Table 2, for ragged contexts).  A NULL
+ *                   array uses the call's scalar for every request.  A negative
+ *                   tok_lo[r] is bad input: it is taken as 0 and sets
+ *                   SPLASH_DEVICE_BAD_INPUT.
+ *   rows            int32 [B] device: request r of the call reads row rows[r] of q,
+ *                   block_table and ctx_lens and writes row rows[r] of out and lse.
+ *                   Those arrays then have num_rows rows.  This lets a DP-attention /
+ *                   DOP owner decode its subset of a batch in place.  The rows must be
+ *                   distinct.  A row outside [0, num_rows) is bad input: nothing is
+ *                   read or written for that request, and SPLASH_DEVICE_BAD_INPUT is set.
+ *   num_rows        rows of q / block_table / ctx_lens / out / lse when rows != NULL
+ *                   (>= 1); ignored otherwise (the arrays then have B rows).
+ */
+typedef struct {
+    const int32_t* tok_lo;
+    const int32_t* tok_hi;
+    const int32_t* rows;
+    int32_t num_rows;
+} splash_decode_ext;
+
+/*
+ * splash_decode_attn with per-request token ranges and storage rows.
+ * `ext` may be NULL.  desc->num_reqs is B, the number of requests in the call
+ * and the length of the ext arrays.  The scalars tok_lo / tok_hi apply to every
+ * request whose array is NULL, and are validated as in splash_decode_attn.  The
+ * workspace size is splash_decode_workspace_size(desc, head_lo, head_hi), as
+ * for splash_decode_attn.  Alignment: the ext arrays 4 bytes.  Otherwise the
+ * same arguments, results and errors as splash_decode_attn.
+ */
+SPLASH_API int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext* ext,
+                          const void* q, const void* kv_pool, const int32_t* block_table,
+                          const int32_t* ctx_lens, int head_lo, int head_hi, int64_t tok_lo,
+                          int64_t tok_hi, float* out, float* lse, void* workspace,
+                          size_t ws_bytes, splash_stream_t stream);
+
+/*
  * splash_decode_attn without a caller workspace.  This entry point has no
  * counterpart in the paper; it exists for callers that cannot allocate device
  * memory at the point where they decode: code inside CUDA stream capture (a

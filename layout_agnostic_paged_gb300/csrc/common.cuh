@@ -42,7 +42,8 @@ struct ReqPlan {
     int32_t first_grp;     // CTA group holding the request's first tile
     int32_t nsplit;        // number of CTA groups the request is cut across (0: empty)
     int32_t slot_base;     // first partial slot (only when nsplit > 1), else -1
-    int32_t pad[2];
+    int32_t row;           // storage row of q / block_table / ctx_lens / out / lse (-1: none)
+    int32_t pad;
 };
 static_assert(sizeof(ReqPlan) == 48, "ReqPlan layout");
 

@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
     for (int r = first_req[j]; r < a.B && req[r].tile_begin < bj; ++r) {
         const ReqPlan p = req[r];
         if (p.ntiles == 0) continue;
+        const int row = p.row;  // storage row of q / block_table / out / lse
         const int64_t t_lo = max(aj, p.tile_begin) - p.tile_begin;
         const int64_t t_hi = min(bj, p.tile_begin + p.ntiles) - p.tile_begin;
         const int split = j - p.first_grp;
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
         for (int i = tid; i < kHG * kDqk; i += kThreads) {
             const int h = i / kDqk, d = i % kDqk;
             sm.q[h][d] = h < nh ? __bfloat162float(
-                                      qg[(int64_t(r) * a.H + a.head_lo + hbase + h) * kDqk + d])
+                                      qg[(int64_t(row) * a.H + a.head_lo + hbase + h) * kDqk + d])
                                 : 0.f;
         }
         if (tid < kHG) {
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
                 const int tok = c0 + t;
                 uint4 val = make_uint4(0u, 0u, 0u, 0u);
                 if (tok < tok_end) {
-                    const int pid = a.block_table[int64_t(r) * a.max_pages + tok / a.P];
+                    const int pid = a.block_table[int64_t(row) * a.max_pages + tok / a.P];
                     if (pid >= 0 && pid < a.num_pages)
                         val = pool[(int64_t(pid) * a.P + tok % a.P) * kVecPerRow + v];
                     else if (v == 0)
@@ -152,8 +153,8 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
             float* dst;
             float* dlse;
             if (p.nsplit == 1) {
-                dst = a.out + (int64_t(r) * a.H + a.head_lo + hh) * kDv;
-                dlse = a.lse + int64_t(r) * a.H + a.head_lo + hh;
+                dst = a.out + (int64_t(row) * a.H + a.head_lo + hh) * kDv;
+                dlse = a.lse + int64_t(row) * a.H + a.head_lo + hh;
             } else {
                 const int64_t slot = p.slot_base + split;
                 dst = pout + (slot * a.Hs + hh) * kDv;

@@ -88,7 +88,8 @@ struct TcParams {
 };
 
 struct Piece {
-    int r;
+    int r;            // request of the call (plan order)
+    int row;          // its storage row in q / block_table / out / lse
     int t_lo, t_hi;   // tiles of the request (relative to its first tile)
     int split;
     bool valid;
@@ -112,6 +113,7 @@ struct PieceIter {
             const int cur = r++;
             if (p.ntiles == 0) continue;
             pc.r = cur;
+            pc.row = p.row;
             pc.t_lo = int(max(aj, p.tile_begin) - p.tile_begin);
             pc.t_hi = int(min(bj, p.tile_begin + p.ntiles) - p.tile_begin);
             pc.split = j - p.first_grp;
@@ -296,14 +298,14 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                 qph ^= 1;
                 if (lane == 0) {
                     if (pw == 0) mbar_arrive_expect_tx(q_full, C::kQBytes);
-                    const int qrow = pc.r * a.H + a.head_lo + hbase;
+                    const int qrow = pc.row * a.H + a.head_lo + hbase;
                     for (int cb = pw; cb < 9; cb += kProducerWarps)
                         tma_load_2d(sQ + cb * NPAD * 128, &map_q, q_full, cb * 64, qrow, pol_q);
                     if (pw == 0) TRACE(3);
                 }
                 __syncwarp();
                 int ttr = -kTraceTile0;
-                const int32_t* bt = a.block_table + int64_t(pc.r) * a.max_pages;
+                const int32_t* bt = a.block_table + int64_t(pc.row) * a.max_pages;
                 for (int t = pc.t_lo; t < pc.t_hi && ok; ++t) {
                     const int tok0 = (p.tile0 + t) * kTileTokens;
                     // lane k < pages_per_tile looks up page k of the tile
@@ -505,7 +507,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
             float lpart[HW];
 #pragma unroll
             for (int h = 0; h < HW; ++h) lpart[h] = 0.f;
-            const int32_t* bt = a.block_table + int64_t(pc.r) * a.max_pages;
+            const int32_t* bt = a.block_table + int64_t(pc.row) * a.max_pages;
             for (int t = pc.t_lo; t < pc.t_hi; ++t) {
                 const bool first = (t == pc.t_lo);
                 const int tok = (p.tile0 + t) * kTileTokens + row;
@@ -655,8 +657,8 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
             float* lbase;
             int64_t hstride;
             if (p.nsplit == 1) {
-                obase = a.out + (int64_t(pc.r) * a.H + a.head_lo + hbase) * kDv;
-                lbase = a.lse + int64_t(pc.r) * a.H + a.head_lo + hbase;
+                obase = a.out + (int64_t(pc.row) * a.H + a.head_lo + hbase) * kDv;
+                lbase = a.lse + int64_t(pc.row) * a.H + a.head_lo + hbase;
             } else {
                 const int64_t slot = p.slot_base + pc.split;
                 obase = pout + (slot * a.Hs + hbase) * kDv;

@@ -42,8 +42,12 @@ struct DecodeArgs {
 // Raises a kernel's dynamic shared-memory limit once per (kernel, device).
 cudaError_t ensure_smem_optin(const void* kernel, int bytes);
 
-cudaError_t launch_plan(const int32_t* ctx_lens, int B, int64_t tok_lo, int64_t tok_hi, int max_ctx,
-                        int num_groups, int Hs, void* ws, cudaStream_t stream);
+// lo_arr / hi_arr (per-request token ranges) and rows (storage row of each request,
+// of num_rows) may be null: then the scalar range applies and request r is row r.
+cudaError_t launch_plan(const int32_t* ctx_lens, int B, int64_t tok_lo, int64_t tok_hi,
+                        const int32_t* lo_arr, const int32_t* hi_arr, const int32_t* rows,
+                        int num_rows, int max_ctx, int num_groups, int Hs, void* ws,
+                        cudaStream_t stream);
 cudaError_t launch_combine(const void* ws, int B, int H, int head_lo, int Hs, int num_groups,
                            float* out, float* lse, cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* part_out, const float* part_lse, int S, int64_t rows,

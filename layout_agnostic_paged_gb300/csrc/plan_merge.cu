@@ -82,7 +82,8 @@ __device__ __forceinline__ ReqPlan request_span(int L, int64_t tok_lo, int64_t t
     p.first_grp = 0;
     p.nsplit = 0;
     p.slot_base = -1;
-    p.pad[0] = p.pad[1] = 0;
+    p.row = -1;
+    p.pad = 0;
     return p;
 }
 
@@ -91,12 +92,15 @@ __device__ __forceinline__ ReqPlan request_span(int L, int64_t tok_lo, int64_t t
 constexpr int kPlanSmemReqs = 8192;
 
 // One CTA.  Every thread owns a contiguous run of requests; the run is recomputed
-// from ctx_lens in each pass (an L1 hit after the first) so that nothing written to
-// global memory is read back, and the group search runs over shared memory.
+// from the inputs in each pass so that nothing written to global memory is read
+// back, and the group search runs over shared memory.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ ctx_lens,
                                                             int B, int64_t tok_lo, int64_t tok_hi,
-                                                            int max_ctx, int num_groups, int Hs,
-                                                            uint8_t* __restrict__ ws) {
+                                                            const int32_t* __restrict__ lo_arr,
+                                                            const int32_t* __restrict__ hi_arr,
+                                                            const int32_t* __restrict__ rows,
+                                                            int num_rows, int max_ctx, int num_groups,
+                                                            int Hs, uint8_t* __restrict__ ws) {
     extern __shared__ int64_t s_end[];  // [B] tile ends, when B <= kPlanSmemReqs
     __shared__ int64_t warp_sums[32];
     __shared__ int64_t s_total;
@@ -112,19 +116,42 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     const int per = (B + kPlanThreads - 1) / kPlanThreads;
     const int r0 = min(B, int(threadIdx.x) * per);
     const int r1 = min(B, r0 + per);
-    auto clipped_len = [&](int r, bool& bad) {
-        int L = ctx_lens[r];
-        if (L < 0 || L > max_ctx) {
+    // Request r of the call: its storage row (rows[r], else r), its context length and
+    // its token range (lo_arr[r] / hi_arr[r], else the call's scalars), clipped.  A row
+    // outside [0, num_rows), a length outside [0, max_ctx] or a negative range start is
+    // bad input (flagged; the row is skipped, the length clamped, the start taken as 0).
+    auto span_of = [&](int r, bool& bad) {
+        int row = rows ? rows[r] : r;
+        int L = 0;
+        if (row < 0 || row >= num_rows) {
             bad = true;
-            L = min(max(L, 0), max_ctx);
+            row = -1;
+        } else {
+            L = ctx_lens[row];
+            if (L < 0 || L > max_ctx) {
+                bad = true;
+                L = min(max(L, 0), max_ctx);
+            }
         }
-        return L;
+        int64_t lo = tok_lo, hi = tok_hi;
+        if (lo_arr) {
+            lo = lo_arr[r];
+            if (lo < 0) {
+                bad = true;
+                lo = 0;
+            }
+        }
+        if (hi_arr) hi = hi_arr[r];
+        ReqPlan p = request_span(L, lo, hi);
+        if (row < 0) p = request_span(0, 0, 0);
+        p.row = row;
+        return p;
     };
 
     // Pass 1: tile counts.
     bool bad = false;
     int64_t my_tiles = 0;
-    for (int r = r0; r < r1; ++r) my_tiles += request_span(clipped_len(r, bad), tok_lo, tok_hi).ntiles;
+    for (int r = r0; r < r1; ++r) my_tiles += span_of(r, bad).ntiles;
     const int64_t incl = block_inclusive_scan(my_tiles, warp_sums);
     if (threadIdx.x == kPlanThreads - 1) s_total = incl;
     __syncthreads();
@@ -139,7 +166,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         int64_t tb = incl - my_tiles;
         bool unused = false;
         for (int r = r0; r < r1; ++r) {
-            const ReqPlan p = request_span(clipped_len(r, unused), tok_lo, tok_hi);
+            const ReqPlan p = span_of(r, unused);
             if (p.ntiles > 0) {
                 const int64_t nsplit = group_of_tile(tb + p.ntiles - 1, T, G) - group_of_tile(tb, T, G) + 1;
                 if (nsplit > 1) my_slots += nsplit;
@@ -154,7 +181,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         int64_t tb = incl - my_tiles, slot = sincl - my_slots;
         bool unused = false;
         for (int r = r0; r < r1; ++r) {
-            ReqPlan p = request_span(clipped_len(r, unused), tok_lo, tok_hi);
+            ReqPlan p = span_of(r, unused);
             p.tile_begin = tb;
             if (p.ntiles > 0) {
                 const int64_t g0 = group_of_tile(tb, T, G);
@@ -278,9 +305,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict_
     const int r = int(row / Hs), hh = int(row % Hs);
     const WorkspaceLayout lay(B, Hs, num_groups);
     const ReqPlan p = reinterpret_cast<const ReqPlan*>(ws + lay.req_off)[r];
-    if (p.nsplit == 1) return;
-    float* o = out + (int64_t(r) * H + head_lo + hh) * kDv;
-    float* l = lse + int64_t(r) * H + head_lo + hh;
+    if (p.nsplit == 1 || p.row < 0) return;
+    float* o = out + (int64_t(p.row) * H + head_lo + hh) * kDv;
+    float* l = lse + int64_t(p.row) * H + head_lo + hh;
     if (p.nsplit == 0) {
         const int lane = threadIdx.x & 31;
         for (int j = lane * 4; j < kDv; j += 128)
@@ -321,15 +348,18 @@ extern "C" __attribute__((visibility("default"))) int splash_ktrace_clear() {
 }
 #endif
 
-cudaError_t launch_plan(const int32_t* ctx_lens, int B, int64_t tok_lo, int64_t tok_hi, int max_ctx,
-                        int num_groups, int Hs, void* ws, cudaStream_t stream) {
+cudaError_t launch_plan(const int32_t* ctx_lens, int B, int64_t tok_lo, int64_t tok_hi,
+                        const int32_t* lo_arr, const int32_t* hi_arr, const int32_t* rows,
+                        int num_rows, int max_ctx, int num_groups, int Hs, void* ws,
+                        cudaStream_t stream) {
     const int smem = B <= kPlanSmemReqs ? B * int(sizeof(int64_t)) : 0;
     if (smem > 48 * 1024) {
         cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(plan_kernel), smem);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), size_t(smem), stream, ctx_lens, B,
-                      tok_lo, tok_hi, max_ctx, num_groups, Hs, static_cast<uint8_t*>(ws));
+                      tok_lo, tok_hi, lo_arr, hi_arr, rows, num_rows, max_ctx, num_groups, Hs,
+                      static_cast<uint8_t*>(ws));
 }
 
 cudaError_t launch_combine(const void* ws, int B, int H, int head_lo, int Hs, int num_groups,

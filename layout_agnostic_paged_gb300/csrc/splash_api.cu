@@ -162,6 +162,15 @@ int splash_decode_attn(const splash_attn_desc* desc, const void* q, const void* 
                        const int32_t* block_table, const int32_t* ctx_lens, int head_lo,
                        int head_hi, int64_t tok_lo, int64_t tok_hi, float* out, float* lse,
                        void* workspace, size_t ws_bytes, splash_stream_t stream_) {
+    return splash_decode_attn_ex(desc, nullptr, q, kv_pool, block_table, ctx_lens, head_lo, head_hi,
+                                 tok_lo, tok_hi, out, lse, workspace, ws_bytes, stream_);
+}
+
+int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext* ext,
+                          const void* q, const void* kv_pool, const int32_t* block_table,
+                          const int32_t* ctx_lens, int head_lo, int head_hi, int64_t tok_lo,
+                          int64_t tok_hi, float* out, float* lse, void* workspace,
+                          size_t ws_bytes, splash_stream_t stream_) {
     int st = validate_desc(desc);
     if (st != SPLASH_OK) return st;
     if (head_lo < 0 || head_hi > desc->num_heads || head_lo >= head_hi) return SPLASH_ERR_INVALID_ARG;
@@ -170,6 +179,12 @@ int splash_decode_attn(const splash_attn_desc* desc, const void* q, const void* 
     if (tok_hi >= (int64_t(1) << 31)) tok_hi = (int64_t(1) << 31) - 1;
     if (!workspace || !aligned(workspace, 256)) return SPLASH_ERR_INVALID_ARG;
     const int B = desc->num_reqs;
+    const int32_t* lo_arr = ext ? ext->tok_lo : nullptr;
+    const int32_t* hi_arr = ext ? ext->tok_hi : nullptr;
+    const int32_t* rows = ext ? ext->rows : nullptr;
+    const int num_rows = rows ? ext->num_rows : B;   // rows of q / block_table / ... / lse
+    if (rows && num_rows < 1) return SPLASH_ERR_INVALID_ARG;
+    if (!aligned(lo_arr, 4) || !aligned(hi_arr, 4) || !aligned(rows, 4)) return SPLASH_ERR_INVALID_ARG;
     if (B > 0) {
         if (!q || !block_table || !ctx_lens || !out || !lse) return SPLASH_ERR_INVALID_ARG;
         if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(block_table, 4) ||
@@ -189,8 +204,8 @@ int splash_decode_attn(const splash_attn_desc* desc, const void* q, const void* 
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const int max_ctx = desc->max_pages_per_req * desc->page_size;
-    if (launch_plan(ctx_lens, B, tok_lo, tok_hi, max_ctx, g.num_groups, Hs, workspace, stream) !=
-        cudaSuccess)
+    if (launch_plan(ctx_lens, B, tok_lo, tok_hi, lo_arr, hi_arr, rows, num_rows, max_ctx,
+                    g.num_groups, Hs, workspace, stream) != cudaSuccess)
         return SPLASH_ERR_CUDA;
     DecodeArgs a;
     a.q = q;
@@ -213,7 +228,7 @@ int splash_decode_attn(const splash_attn_desc* desc, const void* q, const void* 
     } else {
         CUtensorMap mq, mkv;
         const uint32_t qbox = uint32_t(tc_pad_heads(g.group_heads));
-        if (!encode_rows_576(&mq, q, uint64_t(B) * desc->num_heads, qbox)) return SPLASH_ERR_CUDA;
+        if (!encode_rows_576(&mq, q, uint64_t(num_rows) * desc->num_heads, qbox)) return SPLASH_ERR_CUDA;
         // an empty pool still needs a valid map: point it at the workspace (never read,
         // every page id is then out of range)
         const void* kv = desc->num_pages > 0 ? kv_pool : workspace;

@@ -24,7 +24,8 @@ SPLASH_ERR_CUDA = -4
 SPLASH_DEVICE_TIMEOUT = 1
 SPLASH_DEVICE_BAD_INPUT = 2
 
-EXPORTED = ("splash_decode_workspace_size", "splash_decode_attn", "splash_decode_attn_noalloc",
+EXPORTED = ("splash_decode_workspace_size", "splash_decode_attn", "splash_decode_attn_ex",
+            "splash_decode_attn_noalloc",
             "splash_lse_merge", "splash_kv_migrate", "splash_workspace_status",
             "splash_status_string")
 
@@ -40,6 +41,11 @@ class SplashAttnDesc(ctypes.Structure):
                 ("d_qk", ctypes.c_int32), ("d_v", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("num_pages", ctypes.c_int32), ("max_pages_per_req", ctypes.c_int32),
                 ("scale", ctypes.c_float)]
+
+
+class SplashDecodeExt(ctypes.Structure):
+    _fields_ = [("tok_lo", ctypes.c_void_p), ("tok_hi", ctypes.c_void_p),
+                ("rows", ctypes.c_void_p), ("num_rows", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -62,6 +68,9 @@ def load_library(path: str | None = None):
         lib.splash_decode_workspace_size.restype = sz
         lib.splash_decode_attn.argtypes = [dp, vp, vp, vp, vp, i32, i32, i64, i64, vp, vp, vp, sz, vp]
         lib.splash_decode_attn.restype = i32
+        lib.splash_decode_attn_ex.argtypes = [dp, ctypes.POINTER(SplashDecodeExt), vp, vp, vp, vp,
+                                              i32, i32, i64, i64, vp, vp, vp, sz, vp]
+        lib.splash_decode_attn_ex.restype = i32
         lib.splash_decode_attn_noalloc.argtypes = [dp, vp, vp, vp, vp, i32, i32, i64, i64, vp, vp, vp]
         lib.splash_decode_attn_noalloc.restype = i32
         lib.splash_lse_merge.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
@@ -112,9 +121,13 @@ def splash_decode_workspace_size(desc: SplashAttnDesc, head_lo: int, head_hi: in
                                                            int(head_hi)))
 
 
-def decode_workspace(q, kv_pool, block_table, scale, head_lo=0, head_hi=None) -> torch.Tensor:
-    """Allocates (with torch, on q's device) a workspace large enough for the slice."""
+def decode_workspace(q, kv_pool, block_table, scale, head_lo=0, head_hi=None,
+                     num_reqs=None) -> torch.Tensor:
+    """Allocates (with torch, on q's device) a workspace large enough for the slice
+    (num_reqs: requests in the call, when they are a subset of q's rows)."""
     desc = make_desc(q, kv_pool, block_table, scale)
+    if num_reqs is not None:
+        desc.num_reqs = int(num_reqs)
     head_hi = q.shape[1] if head_hi is None else head_hi
     with torch.cuda.device(q.device):
         n = splash_decode_workspace_size(desc, head_lo, head_hi)
@@ -144,6 +157,42 @@ def splash_decode_attn(q: torch.Tensor, kv_pool: torch.Tensor, block_table: torc
             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != SPLASH_OK:
         raise SplashError(rc, "splash_decode_attn")
+
+
+def splash_decode_attn_ex(q: torch.Tensor, kv_pool: torch.Tensor, block_table: torch.Tensor,
+                          ctx_lens: torch.Tensor, head_lo: int, head_hi: int, tok_lo: int,
+                          tok_hi: int, out: torch.Tensor, lse: torch.Tensor,
+                          workspace: torch.Tensor, scale: float, tok_lo_r=None, tok_hi_r=None,
+                          rows=None, stream=None) -> None:
+    """splash_decode_attn with optional per-request token ranges (int32 [B] tensors
+    tok_lo_r / tok_hi_r) and storage rows (int32 [B] tensor `rows` into q, block_table,
+    ctx_lens, out and lse); B is len(rows) when rows is given, else q's rows."""
+    opt = [t for t in (tok_lo_r, tok_hi_r, rows) if t is not None]
+    _check_cuda(q, kv_pool, block_table, ctx_lens, out, lse, workspace, *opt)
+    if (q.dtype != torch.bfloat16 or kv_pool.dtype != torch.bfloat16 or out.dtype != torch.float32
+            or lse.dtype != torch.float32 or block_table.dtype != torch.int32
+            or ctx_lens.dtype != torch.int32 or any(t.dtype != torch.int32 for t in opt)):
+        raise ValueError("splash_decode_attn_ex: dtype mismatch")
+    R, H, _ = q.shape
+    if out.shape != (R, H, 512) or lse.shape != (R, H) or ctx_lens.shape != (R,):
+        raise ValueError("splash_decode_attn_ex: shape mismatch")
+    B = int(rows.numel()) if rows is not None else R
+    if any(t.shape != (B,) for t in opt):
+        raise ValueError("splash_decode_attn_ex: per-request arrays must have one entry per request")
+    desc = make_desc(q, kv_pool, block_table, scale)
+    desc.num_reqs = B
+    ext = SplashDecodeExt(tok_lo_r.data_ptr() if tok_lo_r is not None else None,
+                          tok_hi_r.data_ptr() if tok_hi_r is not None else None,
+                          rows.data_ptr() if rows is not None else None,
+                          R if rows is not None else 0)
+    with torch.cuda.device(q.device):
+        rc = load_library().splash_decode_attn_ex(
+            ctypes.byref(desc), ctypes.byref(ext), _ptr(q), _ptr(kv_pool), _ptr(block_table),
+            _ptr(ctx_lens), int(head_lo), int(head_hi), int(tok_lo), int(tok_hi), _ptr(out),
+            _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream))
+    if rc != SPLASH_OK:
+        raise SplashError(rc, "splash_decode_attn_ex")
 
 
 def splash_decode_attn_noalloc(q: torch.Tensor, kv_pool: torch.Tensor, block_table: torch.Tensor,

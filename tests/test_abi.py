@@ -95,6 +95,28 @@ def test_decode_rejects_bad_arguments(lib, args):
     assert _decode(lib, _desc(), **args) == S.SPLASH_ERR_INVALID_ARG
 
 
+def _decode_ex(lib, desc, ext, head_lo=0, head_hi=8, tok_lo=0, tok_hi=-1):
+    vp = ctypes.c_void_p
+    return lib.splash_decode_attn_ex(ctypes.byref(desc), ext, vp(FAKE), vp(FAKE), vp(FAKE),
+                                     vp(FAKE), head_lo, head_hi, tok_lo, tok_hi, vp(FAKE),
+                                     vp(FAKE), vp(FAKE), 1 << 30, vp(0))
+
+
+@pytest.mark.parametrize("ext", [
+    dict(rows=FAKE, num_rows=0), dict(rows=FAKE, num_rows=-3), dict(tok_lo=FAKE + 2),
+    dict(tok_hi=FAKE + 1), dict(rows=FAKE + 2, num_rows=4),
+])
+def test_decode_ex_rejects_bad_extensions(lib, ext):
+    e = S.SplashDecodeExt(ext.get("tok_lo"), ext.get("tok_hi"), ext.get("rows"),
+                          ext.get("num_rows", 0))
+    assert _decode_ex(lib, _desc(), ctypes.byref(e)) == S.SPLASH_ERR_INVALID_ARG
+
+
+def test_decode_ex_validates_like_decode_without_extension(lib):
+    assert _decode_ex(lib, _desc(), None, head_lo=3, head_hi=3) == S.SPLASH_ERR_INVALID_ARG
+    assert _decode_ex(lib, _desc(d_qk=512), None) == S.SPLASH_ERR_UNSUPPORTED
+
+
 def test_workspace_size_is_zero_for_invalid_shapes(lib):
     assert lib.splash_decode_workspace_size(ctypes.byref(_desc(d_qk=128)), 0, 8) == 0
     assert lib.splash_decode_workspace_size(ctypes.byref(_desc()), 4, 2) == 0
