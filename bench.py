@@ -226,7 +226,7 @@ class Step:
     25%) of the requests' pages into a second pool.
     """
 
-    def __init__(self, w, inp, device):
+    def __init__(self, w, inp, device, ranges=None):
         import torch
         from layout_agnostic_paged_gb300 import splash as S
         from layout_agnostic_paged_gb300 import workloads as W
@@ -259,6 +259,11 @@ class Step:
                                    self.po[i], self.pl[i]))
             self.merge = True
             self.pattern = f"{n} CP token-share calls + LSE merge"
+            if w.per_request_splits:
+                # share i of request r: [L_r i / n, L_r (i + 1) / n), per-request ranges
+                self.ranges = ranges if ranges is not None else W.per_request_ranges(w).to(device)
+                self.pattern = (f"{n} CP calls with per-request token shares "
+                                f"(splash_decode_attn_ex) + LSE merge")
         hs0 = self.calls[0][1] - self.calls[0][0]
         self.ws = S.decode_workspace(inp.q, inp.pool, inp.block_table, w.scale, 0, hs0)
         frac = w.migrate_frac if w.migrate_frac > 0 else 0.25
@@ -269,6 +274,8 @@ class Step:
         self.dst_ids = self.mig.dst_ids.to(device)
         self.pattern += f" + {int(round(100 * frac))}% KV-page handoff ({self.src_ids.numel()} pages)"
         self.launches_per_step = 3 * len(self.calls) + (1 if self.merge else 0) + 1
+        if not hasattr(self, "ranges"):
+            self.ranges = None
         self.page_bytes = int(inp.pool[0].numel() * inp.pool.element_size())
 
     def call_algorithmic(self, c):
@@ -277,7 +284,11 @@ class Step:
         Hs = hh - hl
         toks = pages = 0
         P = self.w.page_size
-        for L in self.w.ctx_lens:
+        i = next(k for k, x in enumerate(self.calls) if x is c)
+        rng = self.ranges[i].cpu().tolist() if self.ranges is not None else None
+        for r, L in enumerate(self.w.ctx_lens):
+            if rng is not None:
+                lo, hi = rng[0][r], rng[1][r]
             a, b = lo, (L if hi < 0 else min(hi, L))
             if b > a:
                 toks += b - a
@@ -288,10 +299,17 @@ class Step:
     def decode(self, c, q=None, bt=None, ctx=None):
         inp = self.inp
         hl, hh, lo, hi, out, lse = c
-        self.S.splash_decode_attn(q if q is not None else inp.q, inp.pool,
-                                  bt if bt is not None else inp.block_table,
-                                  ctx if ctx is not None else inp.ctx_lens, hl, hh, lo, hi,
-                                  out, lse, self.ws, self.w.scale)
+        q = q if q is not None else inp.q
+        bt = bt if bt is not None else inp.block_table
+        ctx = ctx if ctx is not None else inp.ctx_lens
+        if self.ranges is not None:
+            i = next(k for k, x in enumerate(self.calls) if x is c)
+            self.S.splash_decode_attn_ex(q, inp.pool, bt, ctx, hl, hh, 0, -1, out, lse, self.ws,
+                                         self.w.scale, tok_lo_r=self.ranges[i, 0],
+                                         tok_hi_r=self.ranges[i, 1])
+        else:
+            self.S.splash_decode_attn(q, inp.pool, bt, ctx, hl, hh, lo, hi, out, lse, self.ws,
+                                      self.w.scale)
 
     def run(self, q=None, bt=None, ctx=None, decode_events=None, row_events=None):
         """One step.  decode_events: a (start, end) pair recorded around the step's
@@ -366,9 +384,12 @@ def run_ours(args, world, rank, local):
                                device=device, spare_frac=w.spare_frac)
     # q, block table and context lengths share one buffer: the end-to-end leg copies
     # them in with one transfer
-    in_pack, (inp.q, inp.block_table, inp.ctx_lens) = pack(
-        [inp.q, inp.block_table, inp.ctx_lens], device)
-    step = Step(w, inp, device)
+    ins = [inp.q, inp.block_table, inp.ctx_lens]
+    if w.per_request_splits:
+        ins.append(W.per_request_ranges(w))
+    in_pack, views = pack(ins, device)
+    inp.q, inp.block_table, inp.ctx_lens = views[:3]
+    step = Step(w, inp, device, ranges=views[3] if w.per_request_splits else None)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     K, Wm = args.steps, args.warmup
 

@@ -3,7 +3,8 @@ path's tests/benchmark and the fp64 oracle draw their inputs from.
 
 It holds shapes, distributions and page layouts only -- none of the method's
 arithmetic.  The workloads are the five synthetic configurations the hot path is
-specified on (the pages themselves serve GLM-5.3 / DeepSeek-V3.2 with trained
+specified on, plus a ragged CP batch with per-request shares (the pages themselves
+serve GLM-5.3 / DeepSeek-V3.2 with trained
 weights and real prompts, which are not available; see "SPLASH: Switching
 Parallel Layouts of Attention with Seamless Handoff for LLM Serving", Appendix,
 Tables 4-6 for the B=16, 1,024..65,536-token sweeps these shapes stand in for).
@@ -48,6 +49,7 @@ class Workload:
     # ownership slices exercised by the configuration
     head_shards: int = 1          # TP / DOP: number of equal head shards
     token_splits: int = 1         # CP: number of equal contiguous token ranges
+    per_request_splits: bool = False  # CP shares of each request's own length (not one span)
     migrate_frac: float = 0.0     # handoff: fraction of requests whose pages move
     notes: str = ""
 
@@ -93,8 +95,23 @@ def ragged_handoff() -> Workload:
                     migrate_frac=0.25)
 
 
+def ragged_cp() -> Workload:
+    return Workload("ragged CP: 128 requests, ctx log-uniform 512..131072, 128 heads, page 64, "
+                    "8 token shares of each request's own length",
+                    ragged_ctx_lens(128, 512, 131072, seed=1005), 128, 64, seed=1005,
+                    token_splits=8, per_request_splits=True)
+
+
+def per_request_ranges(w: Workload) -> torch.Tensor:
+    """int32 [splits][2][B]: share i of request r is [L_r i / n, L_r (i + 1) / n)
+    (the ideal token partitioning of each request's own context)."""
+    n = max(2, w.token_splits)
+    L = torch.tensor(w.ctx_lens, dtype=torch.int64)
+    return torch.stack([torch.stack([L * i // n, L * (i + 1) // n]) for i in range(n)]).to(torch.int32)
+
+
 ALL = {"tiny": tiny, "full_heads": full_heads, "cp_long": cp_long, "head_shard": head_shard,
-       "ragged_handoff": ragged_handoff}
+       "ragged_handoff": ragged_handoff, "ragged_cp": ragged_cp}
 
 
 @dataclass
