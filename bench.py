@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="full_heads",
                     help="tiny | full_heads | cp_long | head_shard | ragged_handoff")
+    ap.add_argument("--reserved-sms", type=int, default=16,
+                    help="SMs left to the background page migration in the handoff-overlap "
+                         "measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -296,17 +299,19 @@ class Step:
         rows = self.B * Hs
         return algorithmic(Hs, toks, rows, pages)
 
-    def decode(self, c, q=None, bt=None, ctx=None):
+    def decode(self, c, q=None, bt=None, ctx=None, max_sms=0):
         inp = self.inp
         hl, hh, lo, hi, out, lse = c
         q = q if q is not None else inp.q
         bt = bt if bt is not None else inp.block_table
         ctx = ctx if ctx is not None else inp.ctx_lens
-        if self.ranges is not None:
+        if self.ranges is not None or max_sms:
             i = next(k for k, x in enumerate(self.calls) if x is c)
-            self.S.splash_decode_attn_ex(q, inp.pool, bt, ctx, hl, hh, 0, -1, out, lse, self.ws,
-                                         self.w.scale, tok_lo_r=self.ranges[i, 0],
-                                         tok_hi_r=self.ranges[i, 1])
+            rl = self.ranges[i, 0] if self.ranges is not None else None
+            rh = self.ranges[i, 1] if self.ranges is not None else None
+            self.S.splash_decode_attn_ex(q, inp.pool, bt, ctx, hl, hh, lo, hi, out, lse, self.ws,
+                                         self.w.scale, tok_lo_r=rl, tok_hi_r=rh,
+                                         max_sms=max_sms)
         else:
             self.S.splash_decode_attn(q, inp.pool, bt, ctx, hl, hh, lo, hi, out, lse, self.ws,
                                       self.w.scale)
@@ -331,6 +336,24 @@ class Step:
         self.S.splash_kv_migrate(self.inp.pool, self.pool2, self.src_ids, self.dst_ids)
         if row_events is not None:
             row_events["kv_migrate"][1].record()
+
+    def run_background_handoff(self, side2, max_sms, dec_events, join_event):
+        """The step's decode calls on the current stream with at most max_sms SMs, while
+        the handoff's page migration runs on stream side2 (forked from the current
+        stream; joined back at the end).  dec_events brackets the decode calls."""
+        import torch
+        cur = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(cur)
+        side2.wait_event(fork)
+        with torch.cuda.stream(side2):
+            self.S.splash_kv_migrate(self.inp.pool, self.pool2, self.src_ids, self.dst_ids)
+            join_event.record(side2)
+        dec_events[0].record()
+        for c in self.calls:
+            self.decode(c, max_sms=max_sms)
+        dec_events[1].record()
+        cur.wait_event(join_event)
 
     def merge_bytes(self):
         """Bytes splash_lse_merge must move: every share's fp32 rows read once, one written."""
@@ -473,6 +496,52 @@ def run_ours(args, world, rank, local):
                 torch.cuda.synchronize()
                 dec_ms.append(a.elapsed_time(b))
         dec_src = "CUDA events around graph replays of one decode call"
+    # background handoff: the decode calls on all but RESERVED SMs while the page
+    # migration runs on a second stream, against the decode calls alone on every SM
+    handoff = None
+    if len(inst) == max(K, 1):
+        reserved = args.reserved_sms
+        side2 = torch.cuda.Stream(device)
+        g_alone, g_bg, ev_alone, ev_bg, ev_span = [], [], [], [], []
+        for k in range(K):
+            ea = (new_event(), new_event())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                ea[0].record()
+                for c in step.calls:
+                    step.decode(c)
+                ea[1].record()
+            g_alone.append(g)
+            ev_alone.append(ea)
+            eb, es = (new_event(), new_event()), (new_event(), new_event())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                es[0].record()
+                step.run_background_handoff(side2, torch.cuda.get_device_properties(device)
+                                            .multi_processor_count - reserved, eb,
+                                            torch.cuda.Event())
+                es[1].record()
+            g_bg.append(g)
+            ev_bg.append(eb)
+            ev_span.append(es)
+        for graphs_ in (g_alone, g_bg):
+            for k in range(K):
+                flush.zero_()
+                graphs_[k].replay()
+        torch.cuda.synchronize()
+        t_alone = statistics.mean(a.elapsed_time(b) for a, b in ev_alone) * 1e3
+        t_dec_bg = statistics.mean(a.elapsed_time(b) for a, b in ev_bg) * 1e3
+        t_span = statistics.mean(a.elapsed_time(b) for a, b in ev_span) * 1e3
+        t_mig = statistics.mean(row_ev[k]["kv_migrate"][0].elapsed_time(row_ev[k]["kv_migrate"][1])
+                                for k in range(K)) * 1e3
+        handoff = {
+            "reserved_sms": reserved, "migrate_bytes": step.migrate_bytes(),
+            "decode_us_alone": t_alone, "decode_us_with_background_migrate": t_dec_bg,
+            "decode_slowdown_pct": 100.0 * (t_dec_bg - t_alone) / t_alone,
+            "overlapped_us": t_span, "serial_us": t_alone + t_mig,
+            "note": "decode calls with max_sms = SMs - reserved on one stream, splash_kv_migrate "
+                    "on a second stream of the same graph; serial = decode alone + migrate alone",
+        }
     rows_report = {}
     if row_ev[0] is not None:
         mig_us = statistics.mean(row_ev[k]["kv_migrate"][0].elapsed_time(row_ev[k]["kv_migrate"][1])
@@ -553,6 +622,7 @@ def run_ours(args, world, rank, local):
                          "tflops": achieved_tfs,
                          "tensor_frac_of_bf16_peak": achieved_tfs / bf16_peak},
             "other_rows": {k: dict(v, frac_of_hbm=v["gb_s"] / hbm_peak) for k, v in rows_report.items()},
+            "background_handoff": handoff,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -152,12 +152,16 @@ SPLASH_API int splash_decode_attn(const splash_attn_desc* desc, const void* q, c
  *                   read or written for that request, and SPLASH_DEVICE_BAD_INPUT is set.
  *   num_rows        rows of q / block_table / ctx_lens / out / lse when rows != NULL
  *                   (>= 1); ignored otherwise (the arrays then have B rows).
+ *   max_sms         at most this many SMs run the call's persistent decode grid (0: all
+ *                   of them), leaving the rest to work on other streams, e.g. a
+ *                   background splash_kv_migrate of a layout handoff.  Must be >= 0.
  */
 typedef struct {
     const int32_t* tok_lo;
     const int32_t* tok_hi;
     const int32_t* rows;
     int32_t num_rows;
+    int32_t max_sms;
 } splash_decode_ext;
 
 /*

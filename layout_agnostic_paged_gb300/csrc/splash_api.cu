@@ -184,6 +184,8 @@ int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext*
     const int32_t* rows = ext ? ext->rows : nullptr;
     const int num_rows = rows ? ext->num_rows : B;   // rows of q / block_table / ... / lse
     if (rows && num_rows < 1) return SPLASH_ERR_INVALID_ARG;
+    const int max_sms = ext ? ext->max_sms : 0;
+    if (max_sms < 0) return SPLASH_ERR_INVALID_ARG;
     if (!aligned(lo_arr, 4) || !aligned(hi_arr, 4) || !aligned(rows, 4)) return SPLASH_ERR_INVALID_ARG;
     if (B > 0) {
         if (!q || !block_table || !ctx_lens || !out || !lse) return SPLASH_ERR_INVALID_ARG;
@@ -197,7 +199,7 @@ int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext*
     const int sms = sm_count(dev);
     if (sms <= 0) return SPLASH_ERR_CUDA;
     const int Hs = head_hi - head_lo;
-    const Geometry g = decode_geometry(Hs, sms);
+    const Geometry g = decode_geometry(Hs, max_sms > 0 && max_sms < sms ? max_sms : sms);
     const WorkspaceLayout lay(B, Hs, g.num_groups);
     if (ws_bytes < lay.total) return SPLASH_ERR_WORKSPACE;
     if (B == 0) return SPLASH_OK;

@@ -45,7 +45,8 @@ class SplashAttnDesc(ctypes.Structure):
 
 class SplashDecodeExt(ctypes.Structure):
     _fields_ = [("tok_lo", ctypes.c_void_p), ("tok_hi", ctypes.c_void_p),
-                ("rows", ctypes.c_void_p), ("num_rows", ctypes.c_int32)]
+                ("rows", ctypes.c_void_p), ("num_rows", ctypes.c_int32),
+                ("max_sms", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -163,10 +164,11 @@ def splash_decode_attn_ex(q: torch.Tensor, kv_pool: torch.Tensor, block_table: t
                           ctx_lens: torch.Tensor, head_lo: int, head_hi: int, tok_lo: int,
                           tok_hi: int, out: torch.Tensor, lse: torch.Tensor,
                           workspace: torch.Tensor, scale: float, tok_lo_r=None, tok_hi_r=None,
-                          rows=None, stream=None) -> None:
+                          rows=None, max_sms: int = 0, stream=None) -> None:
     """splash_decode_attn with optional per-request token ranges (int32 [B] tensors
-    tok_lo_r / tok_hi_r) and storage rows (int32 [B] tensor `rows` into q, block_table,
-    ctx_lens, out and lse); B is len(rows) when rows is given, else q's rows."""
+    tok_lo_r / tok_hi_r), storage rows (int32 [B] tensor `rows` into q, block_table,
+    ctx_lens, out and lse; B is len(rows) when rows is given, else q's rows) and an SM
+    budget for the decode grid (max_sms, 0 = all)."""
     opt = [t for t in (tok_lo_r, tok_hi_r, rows) if t is not None]
     _check_cuda(q, kv_pool, block_table, ctx_lens, out, lse, workspace, *opt)
     if (q.dtype != torch.bfloat16 or kv_pool.dtype != torch.bfloat16 or out.dtype != torch.float32
@@ -184,7 +186,7 @@ def splash_decode_attn_ex(q: torch.Tensor, kv_pool: torch.Tensor, block_table: t
     ext = SplashDecodeExt(tok_lo_r.data_ptr() if tok_lo_r is not None else None,
                           tok_hi_r.data_ptr() if tok_hi_r is not None else None,
                           rows.data_ptr() if rows is not None else None,
-                          R if rows is not None else 0)
+                          R if rows is not None else 0, int(max_sms))
     with torch.cuda.device(q.device):
         rc = load_library().splash_decode_attn_ex(
             ctypes.byref(desc), ctypes.byref(ext), _ptr(q), _ptr(kv_pool), _ptr(block_table),

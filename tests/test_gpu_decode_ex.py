@@ -30,7 +30,7 @@ def _i32(xs):
 
 
 def _decode_ex(inp, lo=None, hi=None, rows=None, out=None, lse=None, tok_lo=0, tok_hi=-1,
-               head_lo=0, head_hi=None):
+               head_lo=0, head_hi=None, max_sms=0):
     R, H, _ = inp.q.shape
     head_hi = H if head_hi is None else head_hi
     if out is None:
@@ -44,7 +44,7 @@ def _decode_ex(inp, lo=None, hi=None, rows=None, out=None, lse=None, tok_lo=0, t
                             tok_lo, tok_hi, out, lse, ws, W.MLA_SCALE,
                             tok_lo_r=None if lo is None else _i32(lo),
                             tok_hi_r=None if hi is None else _i32(hi),
-                            rows=None if rows is None else _i32(rows))
+                            rows=None if rows is None else _i32(rows), max_sms=max_sms)
     return out, lse, ws
 
 
@@ -143,3 +143,15 @@ def test_bad_row_and_negative_start_are_flagged_and_skipped():
     assert S.splash_workspace_status(ws) & S.SPLASH_DEVICE_BAD_INPUT
     _check_request(inp, out, lse, 0, 0, -1, "negative start taken as 0")
     _check_request(inp, out, lse, 2, 100, -1, "request 2")
+
+
+@pytest.mark.parametrize("max_sms", [1, 7, 16, 100000])
+def test_sm_budget_changes_the_split_not_the_result(max_sms):
+    """A decode grid held to max_sms SMs (the rest left to background work) cuts the
+    tiles differently but computes the same attention."""
+    ctx = [5000, 300, 2048, 129, 64]
+    inp = W.make_decode_inputs(ctx, 128, 64, seed=51, device=DEV)
+    out, lse, ws = _decode_ex(inp, max_sms=max_sms)
+    for r in range(len(ctx)):
+        _check_request(inp, out, lse, r, 0, -1, f"max_sms={max_sms} request {r}")
+    assert S.splash_workspace_status(ws) == 0
