@@ -49,6 +49,9 @@ def _bind(lib):
     lib.oracle_decode_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, dbl, vp, vp, vp, vp,
                                        i32, i32, i64, i64, vp, vp]
     lib.oracle_decode_attn.restype = i32
+    lib.oracle_decode_attn_kv.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, dbl, vp, vp, vp,
+                                          vp, i32, i32, i64, i64, vp, vp]
+    lib.oracle_decode_attn_kv.restype = i32
     lib.oracle_lse_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp]
     lib.oracle_lse_merge.restype = i32
     lib.oracle_kv_migrate.argtypes = [vp, vp, i64, vp, vp, i32, ctypes.c_int32, ctypes.c_int32]
@@ -141,17 +144,22 @@ def decode_attn(q_bits, pool_bits, block_table, ctx_lens, scale: float, head_lo:
                 out: np.ndarray | None = None, lse: np.ndarray | None = None, _lib=None):
     """fp64 paged decode attention of one ownership slice.
 
-    q_bits uint16 [B][H][d_qk], pool_bits uint16 [num_pages][P][d_qk] (bf16 bits),
-    block_table int32 [B][max_pages], ctx_lens int32 [B].  Returns (out, lse) as
-    float64 [B][H][d_v] / [B][H] with d_v = 512 (the latent prefix of the key);
-    rows outside [head_lo, head_hi) are left as given (NaN when freshly made).
+    q_bits uint16 [B][H][d_qk], pool_bits uint16 [num_pages][P][d_qk] (bf16 bits;
+    one shared KV head) or [num_pages][Hkv][P][d_qk] (Hkv KV heads, query head h
+    reading KV head h / (H / Hkv)), block_table int32 [B][max_pages], ctx_lens int32
+    [B].  Returns (out, lse) as float64 [B][H][d_v] / [B][H] with d_v = 512 (the
+    latent prefix of the key); rows outside [head_lo, head_hi) are left as given
+    (NaN when freshly made).
     """
     q = _c(q_bits, np.uint16)
     pool = _c(pool_bits, np.uint16)
     bt = _c(block_table, np.int32)
     cl = _c(ctx_lens, np.int32)
     B, H, d_qk = q.shape
-    num_pages, P, d_qk2 = pool.shape
+    if pool.ndim == 4:
+        num_pages, Hkv, P, d_qk2 = pool.shape
+    else:
+        (num_pages, P, d_qk2), Hkv = pool.shape, 0
     assert d_qk2 == d_qk
     d_v = 512 if d_qk == 576 else d_qk
     if head_hi is None:
@@ -163,7 +171,13 @@ def decode_attn(q_bits, pool_bits, block_table, ctx_lens, scale: float, head_lo:
     assert out.dtype == np.float64 and out.flags.c_contiguous
     assert lse.dtype == np.float64 and lse.flags.c_contiguous
     max_pages = bt.shape[1] if bt.ndim == 2 else 0
-    rc = (_lib or _load()).oracle_decode_attn(B, H, d_qk, d_v, P, num_pages, max_pages, float(scale),
+    lib = _lib or _load()
+    if Hkv:
+        rc = lib.oracle_decode_attn_kv(B, H, Hkv, d_qk, d_v, P, num_pages, max_pages, float(scale),
+                                       _ptr(q), _ptr(pool), _ptr(bt), _ptr(cl), int(head_lo),
+                                       int(head_hi), int(tok_lo), int(tok_hi), _ptr(out), _ptr(lse))
+    else:
+        rc = lib.oracle_decode_attn(B, H, d_qk, d_v, P, num_pages, max_pages, float(scale),
                                     _ptr(q), _ptr(pool), _ptr(bt), _ptr(cl), int(head_lo),
                                     int(head_hi), int(tok_lo), int(tok_hi), _ptr(out), _ptr(lse))
     if rc != 0:

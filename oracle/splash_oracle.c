@@ -83,7 +83,8 @@ void oracle_set_num_threads(int n) {
  * caller passing only that subset's rows.
  *
  *   q           bf16 bits [B][H][d_qk]
- *   pool        bf16 bits [num_pages][P][d_qk]
+ *   pool        bf16 bits [num_pages][P][d_qk] (one shared KV head; see
+ *               oracle_decode_attn_kv for several)
  *   block_table int32 [B][max_pages]
  *   ctx_lens    int32 [B]
  *   out         double [B][H][d_v]; only rows [head_lo, head_hi) are written
@@ -92,14 +93,18 @@ void oracle_set_num_threads(int n) {
  * Returns 0 on success, -1 on an invalid argument (nothing is written then), -2
  * if a block-table entry needed by the slice is outside [0, num_pages).
  */
-int oracle_decode_attn(int B, int H, int d_qk, int d_v, int P, int num_pages, int max_pages,
-                       double scale, const uint16_t* q, const uint16_t* pool,
-                       const int32_t* block_table, const int32_t* ctx_lens, int head_lo,
-                       int head_hi, int64_t tok_lo, int64_t tok_hi, double* out, double* lse) {
-    if (B < 0 || H <= 0 || d_qk <= 0 || d_v <= 0 || d_v > d_qk || P <= 0 || num_pages < 0 ||
-        max_pages < 0 || head_lo < 0 || head_hi > H || head_lo >= head_hi || tok_lo < 0 ||
-        (tok_hi >= 0 && tok_hi < tok_lo))
+/* The same with Hkv key/value heads (grouped-query attention; the Abstract's "few
+ * or no KV heads"): the pool is [num_pages][Hkv][P][d_qk] and query head h reads KV
+ * head h / (H / Hkv).  Hkv = 1 is the shared latent head of MLA. */
+int oracle_decode_attn_kv(int B, int H, int Hkv, int d_qk, int d_v, int P, int num_pages,
+                          int max_pages, double scale, const uint16_t* q, const uint16_t* pool,
+                          const int32_t* block_table, const int32_t* ctx_lens, int head_lo,
+                          int head_hi, int64_t tok_lo, int64_t tok_hi, double* out, double* lse) {
+    if (B < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || d_qk <= 0 || d_v <= 0 || d_v > d_qk ||
+        P <= 0 || num_pages < 0 || max_pages < 0 || head_lo < 0 || head_hi > H ||
+        head_lo >= head_hi || tok_lo < 0 || (tok_hi >= 0 && tok_hi < tok_lo))
         return -1;
+    const int group = H / Hkv;   /* query heads per KV head */
     /* Every page id the slice needs must name a pool page. */
     for (int r = 0; r < B; ++r) {
         int64_t L = ctx_lens[r];
@@ -134,10 +139,11 @@ int oracle_decode_attn(int B, int H, int d_qk, int d_v, int P, int num_pages, in
                 continue;
             }
             const uint16_t* qrow = q + ((int64_t)r * H + h) * d_qk;
+            const int kvh = h / group;
             /* 1. scores s_t = scale * <q, k_t> */
             for (int64_t t = lo; t < hi; ++t) {
                 int32_t page = block_table[(int64_t)r * max_pages + t / P];
-                const uint16_t* k = pool + ((int64_t)page * P + t % P) * d_qk;
+                const uint16_t* k = pool + (((int64_t)page * Hkv + kvh) * P + t % P) * d_qk;
                 double acc = 0.0;
                 for (int d = 0; d < d_qk; ++d) acc += bf16_to_double(qrow[d]) * bf16_to_double(k[d]);
                 s[t - lo] = scale * acc;
@@ -152,7 +158,7 @@ int oracle_decode_attn(int B, int H, int d_qk, int d_v, int P, int num_pages, in
                 double w = exp(s[t - lo] - M);
                 Z += w;
                 int32_t page = block_table[(int64_t)r * max_pages + t / P];
-                const uint16_t* v = pool + ((int64_t)page * P + t % P) * d_qk;
+                const uint16_t* v = pool + (((int64_t)page * Hkv + kvh) * P + t % P) * d_qk;
                 for (int j = 0; j < d_v; ++j) o[j] += w * bf16_to_double(v[j]);
             }
             for (int j = 0; j < d_v; ++j) o[j] /= Z;
@@ -161,6 +167,14 @@ int oracle_decode_attn(int B, int H, int d_qk, int d_v, int P, int num_pages, in
         }
     }
     return status;
+}
+
+int oracle_decode_attn(int B, int H, int d_qk, int d_v, int P, int num_pages, int max_pages,
+                       double scale, const uint16_t* q, const uint16_t* pool,
+                       const int32_t* block_table, const int32_t* ctx_lens, int head_lo,
+                       int head_hi, int64_t tok_lo, int64_t tok_hi, double* out, double* lse) {
+    return oracle_decode_attn_kv(B, H, 1, d_qk, d_v, P, num_pages, max_pages, scale, q, pool,
+                                 block_table, ctx_lens, head_lo, head_hi, tok_lo, tok_hi, out, lse);
 }
 
 /*

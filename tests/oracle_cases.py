@@ -71,3 +71,29 @@ def random_case(rng, ctx_lens, num_heads, page_size, scale_kv=1.0, shuffle=True)
     qb = to_bf16_bits(q)
     toks_exact = [from_bf16_bits(to_bf16_bits(t)) for t in toks]
     return dict(q=qb, pool=pool, bt=bt, ctx=ctx, tokens=toks_exact, page_ids=ids)
+
+
+def random_gqa_case(rng, ctx_lens, num_heads, num_kv_heads, page_size):
+    """Random bf16 q and per-KV-head tokens in a shuffled pool [pages][Hkv][P][576]
+    (NaN in unused slots); tokens[r][j] are request r's KV-head-j rows."""
+    Hkv, P = num_kv_heads, page_size
+    toks = [[rng.standard_normal((L, D_QK)).astype(np.float32) for _ in range(Hkv)]
+            for L in ctx_lens]
+    q = rng.standard_normal((len(ctx_lens), num_heads, D_QK)).astype(np.float32)
+    ppr = [(L + P - 1) // P for L in ctx_lens]
+    used = sum(ppr)
+    perm = rng.permutation(used + 2)
+    pool = np.full((used + 2, Hkv, P, D_QK), np.nan, dtype=np.float32)
+    bt = np.full((len(ctx_lens), max(max(ppr), 1)), -1, dtype=np.int32)
+    k = 0
+    for r, L in enumerate(ctx_lens):
+        for i in range(ppr[r]):
+            pid = int(perm[k])
+            k += 1
+            bt[r, i] = pid
+            for j in range(Hkv):
+                rows = toks[r][j][i * P:(i + 1) * P]
+                pool[pid, j, :rows.shape[0]] = rows
+    exact = [[from_bf16_bits(to_bf16_bits(t)) for t in per_head] for per_head in toks]
+    return dict(q=to_bf16_bits(q), pool=to_bf16_bits(pool), bt=bt,
+                ctx=np.array(ctx_lens, dtype=np.int32), tokens=exact)

@@ -24,8 +24,10 @@ MUTANTS = {
     "wrong_query_head": ("const uint16_t* qrow = q + ((int64_t)r * H + h) * d_qk;",
                          "const uint16_t* qrow = q + ((int64_t)r * H + (H - 1 - h)) * d_qk;"),
     # value gathered from the neighbouring slot of the page
-    "value_slot_off_by_one": ("const uint16_t* v = pool + ((int64_t)page * P + t % P) * d_qk;",
-                              "const uint16_t* v = pool + ((int64_t)page * P + (t + 1) % P) * d_qk;"),
+    "value_slot_off_by_one": ("const uint16_t* v = pool + (((int64_t)page * Hkv + kvh) * P + t % P) * d_qk;",
+                              "const uint16_t* v = pool + (((int64_t)page * Hkv + kvh) * P + (t + 1) % P) * d_qk;"),
+    # query heads mapped to KV heads round-robin instead of in contiguous groups
+    "wrong_kv_head": ("const int kvh = h / group;", "const int kvh = h % Hkv;"),
     # merge forgets to normalise by the summed weights
     "merge_unnormalised": ("for (int j = 0; j < d_v; ++j) o[j] /= W;", ""),
     # merge weights not taken relative to the max (exp(lse) directly, wrong when M != 0)
@@ -46,6 +48,7 @@ def _checks():
         pins.test_two_tokens_sigmoid_weights,
         pins.test_dominant_token_wins,
         lambda: pins.test_matches_torch_sdpa_float64([1, 17, 40], 5, 16),
+        lambda: pins.test_gqa_matches_torch_sdpa_float64([1, 17, 40], 8, 2, 16),
         lambda: pins.test_cp_token_ranges_merge_to_unsplit(2),
         pins.test_merge_weights_closed_form,
         pins.test_merge_equal_parts_adds_ln2,

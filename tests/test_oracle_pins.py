@@ -14,7 +14,8 @@ import pytest
 import torch
 
 import oracle
-from tests.oracle_cases import D_QK, D_V, from_bf16_bits, paged, random_case, to_bf16_bits
+from tests.oracle_cases import (D_QK, D_V, from_bf16_bits, paged, random_case, random_gqa_case,
+                                to_bf16_bits)
 
 SCALE = 1.0 / math.sqrt(192.0)
 
@@ -125,6 +126,47 @@ def test_matches_torch_sdpa_float64(ctx, H, P):
         ref_lse = torch.logsumexp(SCALE * (q[r] @ K.T), dim=-1)
         np.testing.assert_allclose(out[r], ref.numpy(), rtol=0, atol=1e-12)
         np.testing.assert_allclose(lse[r], ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+# --------------------------------------- several KV heads (grouped-query attention)
+
+@pytest.mark.parametrize("ctx,H,Hkv,P", [([1, 17, 40], 8, 2, 16), ([70, 3], 6, 3, 16),
+                                        ([130], 4, 4, 64)])
+def test_gqa_matches_torch_sdpa_float64(ctx, H, Hkv, P):
+    """Query head h attends to KV head h / (H / Hkv): per KV head, SDPA over its
+    group of query heads (the Abstract's "few or no KV heads")."""
+    rng = np.random.default_rng(sum(ctx) + 10 * H + Hkv)
+    case = random_gqa_case(rng, ctx, H, Hkv, P)
+    out, lse = _run(case)
+    q = torch.from_numpy(from_bf16_bits(case["q"]))
+    g = H // Hkv
+    for r, L in enumerate(ctx):
+        for j in range(Hkv):
+            K = torch.from_numpy(case["tokens"][r][j])
+            V = K[:, :D_V]
+            qg = q[r, j * g:(j + 1) * g]                            # [g][576]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qg.unsqueeze(1).unsqueeze(0), K.expand(g, L, D_QK).unsqueeze(0),
+                V.expand(g, L, D_V).unsqueeze(0), scale=SCALE)[0, :, 0, :]
+            ref_lse = torch.logsumexp(SCALE * (qg @ K.T), dim=-1)
+            np.testing.assert_allclose(out[r, j * g:(j + 1) * g], ref.numpy(), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[r, j * g:(j + 1) * g], ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+def test_gqa_with_one_kv_head_is_the_shared_head():
+    rng = np.random.default_rng(11)
+    case = random_case(rng, [33, 70, 5], num_heads=8, page_size=16)
+    o3, l3 = _run(case)
+    four = dict(case, pool=case["pool"][:, None])          # [pages][1][P][576]
+    o4, l4 = _run(four)
+    assert np.array_equal(o3, o4) and np.array_equal(l3, l4)
+
+
+def test_gqa_rejects_heads_not_divisible_by_kv_heads():
+    rng = np.random.default_rng(12)
+    case = random_gqa_case(rng, [10], 6, 4, 16)
+    with pytest.raises(ValueError):
+        _run(case)
 
 
 # ------------------------------------------ invariants of the layouts (Table 2)
