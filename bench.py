@@ -297,7 +297,10 @@ class Step:
                 toks += b - a
                 pages += (b - 1) // P - a // P + 1
         rows = self.B * Hs
-        return algorithmic(Hs, toks, rows, pages)
+        # with several KV heads a call reads the KV heads its query heads map to
+        Hkv = self.w.num_kv_heads
+        kv_read = 1 if Hkv == 1 else len({h // (self.H // Hkv) for h in range(hl, hh)})
+        return algorithmic(Hs, toks, rows, pages, kv_read)
 
     def decode(self, c, q=None, bt=None, ctx=None, max_sms=0):
         inp = self.inp
@@ -305,7 +308,7 @@ class Step:
         q = q if q is not None else inp.q
         bt = bt if bt is not None else inp.block_table
         ctx = ctx if ctx is not None else inp.ctx_lens
-        if self.ranges is not None or max_sms:
+        if self.ranges is not None or max_sms or inp.pool.dim() == 4:
             i = next(k for k, x in enumerate(self.calls) if x is c)
             rl = self.ranges[i, 0] if self.ranges is not None else None
             rh = self.ranges[i, 1] if self.ranges is not None else None
@@ -383,10 +386,12 @@ def pack(tensors, device):
     return buf, views
 
 
-def algorithmic(Hs, tokens_in_call, rows, pages):
-    """Bytes and flops one decode call must move / do: every KV token once (576 bf16),
-    q rows (576 bf16), fp32 out rows + lse, 4 bytes per page id."""
-    bytes_ = tokens_in_call * 576 * 2 + rows * 576 * 2 + rows * (512 * 4 + 4) + pages * 4
+def algorithmic(Hs, tokens_in_call, rows, pages, kv_heads_read=1):
+    """Bytes and flops one decode call must move / do: every KV token once (576 bf16
+    per KV head the call reads), q rows (576 bf16), fp32 out rows + lse, 4 bytes per
+    page id."""
+    bytes_ = (tokens_in_call * 576 * 2 * kv_heads_read + rows * 576 * 2 + rows * (512 * 4 + 4)
+              + pages * 4)
     flops = 2.0 * tokens_in_call * Hs * (576 + 512)
     return bytes_, flops
 
@@ -404,7 +409,7 @@ def run_ours(args, world, rank, local):
     w = W.ALL[args.workload]()
     # weak scaling: every rank owns its own batch of the workload (own seed)
     inp = W.make_decode_inputs(w.ctx_lens, w.num_heads, w.page_size, w.seed + 1000 * rank,
-                               device=device, spare_frac=w.spare_frac)
+                               device=device, spare_frac=w.spare_frac, num_kv_heads=w.num_kv_heads)
     # q, block table and context lengths share one buffer: the end-to-end leg copies
     # them in with one transfer
     ins = [inp.q, inp.block_table, inp.ctx_lens]
@@ -663,7 +668,8 @@ def run_reference(args, world, rank, local):
     from layout_agnostic_paged_gb300 import workloads as W
     w = W.ALL[args.workload]()
     inp = W.make_decode_inputs(w.ctx_lens, w.num_heads, w.page_size, w.seed, device="cpu"
-                               if w.kv_tokens <= 2_000_000 else "cuda:0", spare_frac=w.spare_frac)
+                               if w.kv_tokens <= 2_000_000 else "cuda:0", spare_frac=w.spare_frac,
+                               num_kv_heads=w.num_kv_heads)
     q = oracle.bf16_bits(inp.q)
     pool = oracle.bf16_bits(inp.pool)
     bt = inp.block_table.cpu().numpy()

@@ -155,6 +155,12 @@ SPLASH_API int splash_decode_attn(const splash_attn_desc* desc, const void* q, c
  *   max_sms         at most this many SMs run the call's persistent decode grid (0: all
  *                   of them), leaving the rest to work on other streams, e.g. a
  *                   background splash_kv_migrate of a layout handoff.  Must be >= 0.
+ *   num_kv_heads    KV heads per token, Hkv (0 or 1: the one shared latent head).  With
+ *                   Hkv > 1 (grouped-query attention, the Abstract's "few KV heads") the
+ *                   pool is bf16 [num_pages][Hkv][P][576] and query head h reads KV head
+ *                   h / (H / Hkv).  H must be a multiple of Hkv.  H / Hkv must be at most 64
+ *                   or a multiple of 64, and head_lo a multiple of min(H / Hkv, 64); other
+ *                   shapes return SPLASH_ERR_UNSUPPORTED, as does the CUDA-core kernel.
  */
 typedef struct {
     const int32_t* tok_lo;
@@ -162,6 +168,7 @@ typedef struct {
     const int32_t* rows;
     int32_t num_rows;
     int32_t max_sms;
+    int32_t num_kv_heads;
 } splash_decode_ext;
 
 /*

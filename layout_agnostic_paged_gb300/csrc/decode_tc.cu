@@ -235,6 +235,9 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
     const int nh = min(prm.group_heads, a.Hs - hbase);      // valid heads of the group
     const int P = a.P;
     const int pages_per_tile = kTileTokens / P;
+    // the head group lies within one KV head's group of query heads (checked on the
+    // host); page p of that KV head starts at row (p * kv_heads + kvh) * P of the pool
+    const int kvh = a.kv_heads > 1 ? (a.head_lo + hbase) / a.q_per_kv : 0;
 
     // Prologue (overlaps the plan kernel under programmatic dependent launch).
     if (threadIdx.x == 0) TRACE(0);
@@ -343,7 +346,8 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                                 for (int c2 = 0; c2 < 2; ++c2)
                                     if ((g0 + 2 * lane + c2) % kProducerWarps == pw)
                                         tma_load_2d(slot + c2 * kColBlockBytes + lane * P * 128, &map_kv,
-                                                    &pair_full[ps], (2 * jj + c2) * 64, my_pid * P, pol_kv);
+                                                    &pair_full[ps], (2 * jj + c2) * 64,
+                                                    (my_pid * a.kv_heads + kvh) * P, pol_kv);
                             __syncwarp();
                         }
                         if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
@@ -358,7 +362,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                         __syncwarp();
                         if (my_pid >= 0 && (g0 + lane) % kProducerWarps == pw)
                             tma_load_2d(sRope + rs * kColBlockBytes + lane * P * 128, &map_kv,
-                                        &rope_full[rs], 8 * 64, my_pid * P, pol_kv);
+                                        &rope_full[rs], 8 * 64, (my_pid * a.kv_heads + kvh) * P, pol_kv);
                         __syncwarp();
                         if (pw == g0 % kProducerWarps && lane == 0 && unsigned(ttr) < 3u)
                             TRACE(6 + ttr * 3);

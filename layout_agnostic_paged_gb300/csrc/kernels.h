@@ -28,7 +28,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Arguments of one decode-kernel launch (device pointers, already validated).
 struct DecodeArgs {
     const void* q;              // bf16 [B][H][576]
-    const void* kv_pool;        // bf16 [num_pages][P][576]
+    const void* kv_pool;        // bf16 [num_pages][kv_heads][P][576]
     const int32_t* block_table; // [B][max_pages]
     float* out;                 // [B][H][512]
     float* lse;                 // [B][H]
@@ -36,6 +36,8 @@ struct DecodeArgs {
     int B, H, P, num_pages, max_pages;
     int head_lo, Hs;            // head slice
     int num_groups;             // CTA groups G'
+    int kv_heads;               // KV heads per token (1: the shared latent head)
+    int q_per_kv;               // query heads per KV head (H / kv_heads)
     float scale;
 };
 

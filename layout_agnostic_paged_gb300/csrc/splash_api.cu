@@ -66,12 +66,18 @@ struct Geometry {
     int num_groups;   // CTA groups G' (the tile sequence is cut into G' ranges)
 };
 
-Geometry decode_geometry(int Hs, int sms) {
+// kv_group_heads > 0 forces head groups of that size (several KV heads: a group must
+// stay within one KV head's query heads).
+Geometry decode_geometry(int Hs, int sms, int kv_group_heads = 0) {
     Geometry g;
     if (use_simt()) {
         g.head_groups = (Hs + kSimtHeads - 1) / kSimtHeads;
         g.group_heads = kSimtHeads;
         g.num_groups = (2 * sms) / g.head_groups;
+    } else if (kv_group_heads > 0) {
+        g.group_heads = kv_group_heads;
+        g.head_groups = (Hs + kv_group_heads - 1) / kv_group_heads;
+        g.num_groups = sms / g.head_groups;
     } else {
         g.head_groups = (Hs + kTcMaxGroupHeads - 1) / kTcMaxGroupHeads;
         g.group_heads = (Hs + g.head_groups - 1) / g.head_groups;
@@ -186,6 +192,18 @@ int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext*
     if (rows && num_rows < 1) return SPLASH_ERR_INVALID_ARG;
     const int max_sms = ext ? ext->max_sms : 0;
     if (max_sms < 0) return SPLASH_ERR_INVALID_ARG;
+    const int kv_heads = ext && ext->num_kv_heads > 1 ? ext->num_kv_heads : 1;
+    if (ext && ext->num_kv_heads < 0) return SPLASH_ERR_INVALID_ARG;
+    int kv_group_heads = 0;   // head-group size forced by several KV heads
+    if (kv_heads > 1) {
+        if (desc->num_heads % kv_heads != 0) return SPLASH_ERR_INVALID_ARG;
+        const int per_kv = desc->num_heads / kv_heads;
+        if (per_kv > kTcMaxGroupHeads && per_kv % kTcMaxGroupHeads != 0) return SPLASH_ERR_UNSUPPORTED;
+        kv_group_heads = per_kv < kTcMaxGroupHeads ? per_kv : kTcMaxGroupHeads;
+        if (head_lo % kv_group_heads != 0 || use_simt()) return SPLASH_ERR_UNSUPPORTED;
+        if (int64_t(desc->num_pages) * kv_heads * desc->page_size >= (int64_t(1) << 31))
+            return SPLASH_ERR_UNSUPPORTED;
+    }
     if (!aligned(lo_arr, 4) || !aligned(hi_arr, 4) || !aligned(rows, 4)) return SPLASH_ERR_INVALID_ARG;
     if (B > 0) {
         if (!q || !block_table || !ctx_lens || !out || !lse) return SPLASH_ERR_INVALID_ARG;
@@ -199,7 +217,8 @@ int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext*
     const int sms = sm_count(dev);
     if (sms <= 0) return SPLASH_ERR_CUDA;
     const int Hs = head_hi - head_lo;
-    const Geometry g = decode_geometry(Hs, max_sms > 0 && max_sms < sms ? max_sms : sms);
+    const Geometry g = decode_geometry(Hs, max_sms > 0 && max_sms < sms ? max_sms : sms,
+                                       kv_group_heads);
     const WorkspaceLayout lay(B, Hs, g.num_groups);
     if (ws_bytes < lay.total) return SPLASH_ERR_WORKSPACE;
     if (B == 0) return SPLASH_OK;
@@ -224,6 +243,8 @@ int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext*
     a.head_lo = head_lo;
     a.Hs = Hs;
     a.num_groups = g.num_groups;
+    a.kv_heads = kv_heads;
+    a.q_per_kv = desc->num_heads / kv_heads;
     a.scale = desc->scale;
     if (use_simt()) {
         if (launch_decode_simt(a, stream) != cudaSuccess) return SPLASH_ERR_CUDA;
@@ -234,8 +255,9 @@ int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext*
         // an empty pool still needs a valid map: point it at the workspace (never read,
         // every page id is then out of range)
         const void* kv = desc->num_pages > 0 ? kv_pool : workspace;
-        const uint64_t kv_rows = desc->num_pages > 0 ? uint64_t(desc->num_pages) * desc->page_size
-                                                     : uint64_t(1);
+        const uint64_t kv_rows = desc->num_pages > 0
+                                     ? uint64_t(desc->num_pages) * kv_heads * desc->page_size
+                                     : uint64_t(1);
         if (!encode_rows_576(&mkv, kv, kv_rows, uint32_t(desc->page_size))) return SPLASH_ERR_CUDA;
         if (launch_decode_tc(a, mq, mkv, g.head_groups, g.group_heads, stream) != cudaSuccess)
             return SPLASH_ERR_CUDA;

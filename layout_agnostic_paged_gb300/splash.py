@@ -46,7 +46,7 @@ class SplashAttnDesc(ctypes.Structure):
 class SplashDecodeExt(ctypes.Structure):
     _fields_ = [("tok_lo", ctypes.c_void_p), ("tok_hi", ctypes.c_void_p),
                 ("rows", ctypes.c_void_p), ("num_rows", ctypes.c_int32),
-                ("max_sms", ctypes.c_int32)]
+                ("max_sms", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -111,7 +111,10 @@ def _check_cuda(*ts):
 def make_desc(q: torch.Tensor, kv_pool: torch.Tensor, block_table: torch.Tensor,
               scale: float) -> SplashAttnDesc:
     B, H, d_qk = q.shape
-    num_pages, P, d_qk2 = kv_pool.shape
+    if kv_pool.dim() == 4:   # [num_pages][Hkv][P][576]: several KV heads
+        num_pages, _, P, d_qk2 = kv_pool.shape
+    else:
+        num_pages, P, d_qk2 = kv_pool.shape
     if d_qk2 != d_qk:
         raise ValueError("q and kv_pool disagree on the key width")
     return SplashAttnDesc(B, H, d_qk, 512, P, num_pages, block_table.shape[1], float(scale))
@@ -143,6 +146,9 @@ def splash_decode_attn(q: torch.Tensor, kv_pool: torch.Tensor, block_table: torc
                        workspace: torch.Tensor, scale: float, stream=None) -> None:
     """Paged decode attention of one ownership slice (see splash.h); writes out / lse rows."""
     _check_cuda(q, kv_pool, block_table, ctx_lens, out, lse, workspace)
+    if kv_pool.dim() != 3:
+        raise ValueError("splash_decode_attn: one shared KV head [num_pages][P][576]; "
+                         "use splash_decode_attn_ex for several KV heads")
     if (q.dtype != torch.bfloat16 or kv_pool.dtype != torch.bfloat16 or out.dtype != torch.float32
             or lse.dtype != torch.float32 or block_table.dtype != torch.int32
             or ctx_lens.dtype != torch.int32):
@@ -168,7 +174,8 @@ def splash_decode_attn_ex(q: torch.Tensor, kv_pool: torch.Tensor, block_table: t
     """splash_decode_attn with optional per-request token ranges (int32 [B] tensors
     tok_lo_r / tok_hi_r), storage rows (int32 [B] tensor `rows` into q, block_table,
     ctx_lens, out and lse; B is len(rows) when rows is given, else q's rows) and an SM
-    budget for the decode grid (max_sms, 0 = all)."""
+    budget for the decode grid (max_sms, 0 = all).  A kv_pool of shape
+    [num_pages][Hkv][P][576] selects grouped-query attention over Hkv KV heads."""
     opt = [t for t in (tok_lo_r, tok_hi_r, rows) if t is not None]
     _check_cuda(q, kv_pool, block_table, ctx_lens, out, lse, workspace, *opt)
     if (q.dtype != torch.bfloat16 or kv_pool.dtype != torch.bfloat16 or out.dtype != torch.float32
@@ -186,7 +193,8 @@ def splash_decode_attn_ex(q: torch.Tensor, kv_pool: torch.Tensor, block_table: t
     ext = SplashDecodeExt(tok_lo_r.data_ptr() if tok_lo_r is not None else None,
                           tok_hi_r.data_ptr() if tok_hi_r is not None else None,
                           rows.data_ptr() if rows is not None else None,
-                          R if rows is not None else 0, int(max_sms))
+                          R if rows is not None else 0, int(max_sms),
+                          int(kv_pool.shape[1]) if kv_pool.dim() == 4 else 0)
     with torch.cuda.device(q.device):
         rc = load_library().splash_decode_attn_ex(
             ctypes.byref(desc), ctypes.byref(ext), _ptr(q), _ptr(kv_pool), _ptr(block_table),

@@ -50,6 +50,7 @@ class Workload:
     head_shards: int = 1          # TP / DOP: number of equal head shards
     token_splits: int = 1         # CP: number of equal contiguous token ranges
     per_request_splits: bool = False  # CP shares of each request's own length (not one span)
+    num_kv_heads: int = 1         # KV heads per token (1: the shared latent head)
     migrate_frac: float = 0.0     # handoff: fraction of requests whose pages move
     notes: str = ""
 
@@ -102,6 +103,11 @@ def ragged_cp() -> Workload:
                     token_splits=8, per_request_splits=True)
 
 
+def gqa() -> Workload:
+    return Workload("grouped-query decode: B=16, ctx 8192, 128 query heads over 8 KV heads, "
+                    "page 64", (8192,) * 16, 128, 64, seed=1006, token_splits=2, num_kv_heads=8)
+
+
 def per_request_ranges(w: Workload) -> torch.Tensor:
     """int32 [splits][2][B]: share i of request r is [L_r i / n, L_r (i + 1) / n)
     (the ideal token partitioning of each request's own context)."""
@@ -111,7 +117,7 @@ def per_request_ranges(w: Workload) -> torch.Tensor:
 
 
 ALL = {"tiny": tiny, "full_heads": full_heads, "cp_long": cp_long, "head_shard": head_shard,
-       "ragged_handoff": ragged_handoff, "ragged_cp": ragged_cp}
+       "ragged_handoff": ragged_handoff, "ragged_cp": ragged_cp, "gqa": gqa}
 
 
 @dataclass
@@ -141,7 +147,7 @@ def _gen(device, seed: int) -> torch.Generator:
 def make_decode_inputs(ctx_lens, num_heads: int, page_size: int, seed: int, device="cpu",
                        spare_frac: float = 0.10, perm_seed: int | None = None,
                        poison: bool = True, max_pages: int | None = None,
-                       chunk_pages: int = 4096) -> DecodeInputs:
+                       chunk_pages: int = 4096, num_kv_heads: int = 1) -> DecodeInputs:
     """Build q, a shuffled paged KV pool and block tables for the given lengths.
 
     The logical KV content depends only on ``seed`` (and the lengths), the
@@ -169,12 +175,15 @@ def make_decode_inputs(ctx_lens, num_heads: int, page_size: int, seed: int, devi
     q = torch.randn((B, num_heads, D_QK), generator=g_q, device=device,
                     dtype=torch.float32).to(torch.bfloat16)
 
-    pool = torch.empty((num_pages, P, D_QK), dtype=torch.bfloat16, device=device)
+    # one KV head: [num_pages][P][576]; several: [num_pages][Hkv][P][576]
+    page_shape = (P, D_QK) if num_kv_heads == 1 else (num_kv_heads, P, D_QK)
+    pool = torch.empty((num_pages,) + page_shape, dtype=torch.bfloat16, device=device)
     g_kv = _gen(device, seed + 7)
     perm_dev = perm.to(device)
-    for k0 in range(0, used, chunk_pages):
-        k1 = min(used, k0 + chunk_pages)
-        chunk = torch.randn((k1 - k0, P, D_QK), generator=g_kv, device=device,
+    step = max(1, chunk_pages // num_kv_heads)
+    for k0 in range(0, used, step):
+        k1 = min(used, k0 + step)
+        chunk = torch.randn((k1 - k0,) + page_shape, generator=g_kv, device=device,
                             dtype=torch.float32).to(torch.bfloat16)
         pool[perm_dev[k0:k1]] = chunk
     if spare:
@@ -192,7 +201,10 @@ def make_decode_inputs(ctx_lens, num_heads: int, page_size: int, seed: int, devi
         k += n
     if poison:
         for pid, rem in tails:
-            pool[pid, rem:] = float("nan")
+            if num_kv_heads == 1:
+                pool[pid, rem:] = float("nan")
+            else:
+                pool[pid, :, rem:] = float("nan")
     return DecodeInputs(q=q, pool=pool, block_table=bt.to(device),
                         ctx_lens=torch.tensor(ctx, dtype=torch.int32, device=device), perm=perm,
                         pages_per_req=ppr)
@@ -200,7 +212,7 @@ def make_decode_inputs(ctx_lens, num_heads: int, page_size: int, seed: int, devi
 
 def make_workload_inputs(w: Workload, device="cpu", **kw) -> DecodeInputs:
     return make_decode_inputs(w.ctx_lens, w.num_heads, w.page_size, w.seed, device=device,
-                              spare_frac=w.spare_frac, **kw)
+                              spare_frac=w.spare_frac, num_kv_heads=w.num_kv_heads, **kw)
 
 
 @dataclass

@@ -104,12 +104,19 @@ def _decode_ex(lib, desc, ext, head_lo=0, head_hi=8, tok_lo=0, tok_hi=-1):
 
 @pytest.mark.parametrize("ext", [
     dict(rows=FAKE, num_rows=0), dict(rows=FAKE, num_rows=-3), dict(tok_lo=FAKE + 2),
-    dict(tok_hi=FAKE + 1), dict(rows=FAKE + 2, num_rows=4), dict(max_sms=-1),
+    dict(tok_hi=FAKE + 1), dict(rows=FAKE + 2, num_rows=4), dict(max_sms=-1), dict(kv=-1),
+    dict(kv=3),   # 8 query heads over 3 KV heads
 ])
 def test_decode_ex_rejects_bad_extensions(lib, ext):
     e = S.SplashDecodeExt(ext.get("tok_lo"), ext.get("tok_hi"), ext.get("rows"),
-                          ext.get("num_rows", 0), ext.get("max_sms", 0))
+                          ext.get("num_rows", 0), ext.get("max_sms", 0), ext.get("kv", 0))
     assert _decode_ex(lib, _desc(), ctypes.byref(e)) == S.SPLASH_ERR_INVALID_ARG
+
+
+def test_decode_ex_rejects_unsupported_kv_head_groupings(lib):
+    e = S.SplashDecodeExt(None, None, None, 0, 0, 2)
+    # 8 query heads over 2 KV heads: groups of 4, so head_lo must be a multiple of 4
+    assert _decode_ex(lib, _desc(), ctypes.byref(e), head_lo=2, head_hi=8) == S.SPLASH_ERR_UNSUPPORTED
 
 
 def test_decode_ex_validates_like_decode_without_extension(lib):
