@@ -6,7 +6,8 @@ One step = one pass of every hot-path row over one synthetic batch (by default
 the full-heads workload: B=16, ctx 1,024, 128 query heads, one shared 576-wide
 latent KV head, page 64, shuffled page ids):
   * CP layout: two token-share decode calls ([0, L/2) and [L/2, L)), each = split
-    plan + tensor-core decode + split combine, producing partial out + LSE;
+    plan + tensor-core decode + split combine, producing partial out + LSE; the
+    calls are independent and alternate between two streams, one workspace each;
   * splash_lse_merge of the two shares into the final out / LSE;
   * a layout handoff: splash_kv_migrate of 25% of the requests' pages into a
     second block pool (the migrated requests' block-table rows are prepared once;
@@ -15,9 +16,11 @@ value = KV tokens of the batch / step time (each KV token is read once per step)
 
 Timing: W untimed warm-up steps, then K timed steps; before every step a 512 MB
 buffer is written to flush the 129 MB L2 (outside the timed events); each step
-is bracketed by CUDA events on the launching stream and the K step times are
-summed; ranks meet at a barrier (+ synchronize) before and after and the max
-over ranks is reported.  `--impl reference` times the fp64 C oracle instead.
+is one CUDA graph replay bracketed by CUDA events on the launching stream and the
+K step times are summed; ranks meet at a barrier (+ synchronize) before and after
+and the max over ranks is reported.  A second pass of instrumented graphs gives
+the per-row breakdown, and a third the decode calls with a background page
+migration.  `--impl reference` times the fp64 C oracle instead.
 """
 from __future__ import annotations
 
@@ -269,6 +272,11 @@ class Step:
                                 f"(splash_decode_attn_ex) + LSE merge")
         hs0 = self.calls[0][1] - self.calls[0][0]
         self.ws = S.decode_workspace(inp.q, inp.pool, inp.block_table, w.scale, 0, hs0)
+        # the step's decode calls are independent: odd calls go to a second stream with a
+        # workspace of their own, so one call's tail overlaps the next call's start
+        self.ws_b = (S.decode_workspace(inp.q, inp.pool, inp.block_table, w.scale, 0, hs0)
+                     if len(self.calls) > 1 else None)
+        self.stream_b = torch.cuda.Stream(device)
         frac = w.migrate_frac if w.migrate_frac > 0 else 0.25
         self.mig = W.make_migration(inp, frac, seed=w.seed)
         self.pool2 = torch.empty((self.mig.dst_num_pages,) + tuple(inp.pool.shape[1:]),
@@ -276,6 +284,8 @@ class Step:
         self.src_ids = self.mig.src_ids.to(device)
         self.dst_ids = self.mig.dst_ids.to(device)
         self.pattern += f" + {int(round(100 * frac))}% KV-page handoff ({self.src_ids.numel()} pages)"
+        if len(self.calls) > 1:
+            self.pattern += "; decode calls alternate between two streams, one workspace each"
         self.launches_per_step = 3 * len(self.calls) + (1 if self.merge else 0) + 1
         if not hasattr(self, "ranges"):
             self.ranges = None
@@ -302,8 +312,9 @@ class Step:
         kv_read = 1 if Hkv == 1 else len({h // (self.H // Hkv) for h in range(hl, hh)})
         return algorithmic(Hs, toks, rows, pages, kv_read)
 
-    def decode(self, c, q=None, bt=None, ctx=None, max_sms=0):
+    def decode(self, c, q=None, bt=None, ctx=None, max_sms=0, ws=None):
         inp = self.inp
+        ws = self.ws if ws is None else ws
         hl, hh, lo, hi, out, lse = c
         q = q if q is not None else inp.q
         bt = bt if bt is not None else inp.block_table
@@ -312,20 +323,34 @@ class Step:
             i = next(k for k, x in enumerate(self.calls) if x is c)
             rl = self.ranges[i, 0] if self.ranges is not None else None
             rh = self.ranges[i, 1] if self.ranges is not None else None
-            self.S.splash_decode_attn_ex(q, inp.pool, bt, ctx, hl, hh, lo, hi, out, lse, self.ws,
+            self.S.splash_decode_attn_ex(q, inp.pool, bt, ctx, hl, hh, lo, hi, out, lse, ws,
                                          self.w.scale, tok_lo_r=rl, tok_hi_r=rh,
                                          max_sms=max_sms)
         else:
-            self.S.splash_decode_attn(q, inp.pool, bt, ctx, hl, hh, lo, hi, out, lse, self.ws,
+            self.S.splash_decode_attn(q, inp.pool, bt, ctx, hl, hh, lo, hi, out, lse, ws,
                                       self.w.scale)
 
     def run(self, q=None, bt=None, ctx=None, decode_events=None, row_events=None):
         """One step.  decode_events: a (start, end) pair recorded around the step's
         back-to-back decode calls; row_events: pairs around the merge and the migration."""
+        import torch
         if decode_events is not None:
             decode_events[0].record()
-        for c in self.calls:
-            self.decode(c, q, bt, ctx)
+        cur = torch.cuda.current_stream()
+        if len(self.calls) > 1:
+            fork = torch.cuda.Event()
+            fork.record(cur)
+            self.stream_b.wait_event(fork)
+        for k, c in enumerate(self.calls):
+            if k % 2:
+                with torch.cuda.stream(self.stream_b):
+                    self.decode(c, q, bt, ctx, ws=self.ws_b)
+            else:
+                self.decode(c, q, bt, ctx)
+        if len(self.calls) > 1:
+            join = torch.cuda.Event()
+            join.record(self.stream_b)
+            cur.wait_event(join)
         if decode_events is not None:
             decode_events[1].record()
         if self.merge:
@@ -560,6 +585,8 @@ def run_ours(args, world, rank, local):
                                         "gb_s": step.merge_bytes() / mer_us / 1e3}
     total_ms = max_over_ranks(sum(step_ms), world, device)
     status = S.splash_workspace_status(step.ws)
+    if step.ws_b is not None:
+        status |= S.splash_workspace_status(step.ws_b)
     if status != 0:
         raise RuntimeError(f"device status word set: {status}")
 
