@@ -83,6 +83,7 @@ struct TcConfig {
 struct TcParams {
     DecodeArgs a;
     float c_log2;        // scale * log2(e): scores in the exp2 domain
+    int keep_kv;         // KV loads marked evict-last (a call whose cache fits in L2)
     int group_heads;     // Gs: heads per head group (the last group may have fewer)
     int head_groups;     // NG
 };
@@ -289,7 +290,9 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
         // belong to producer warp k % kProducerWarps, whose lanes issue them.
         const int pw = warp == 0 ? 0 : warp - C::kFirstExtraProducer + 1;
         if (aj < bj) {
-            const uint64_t pol_kv = policy_evict_first();
+            // a small cache stays in L2 for the next kernels (the sibling head group, a
+            // handoff, the next call); a large stream must not push everything else out
+            const uint64_t pol_kv = prm.keep_kv ? policy_evict_last() : policy_evict_first();
             const uint64_t pol_q = policy_evict_last();
             int ps = 0, pph = 0, rs = 0, rph = 0, qph = 0;
             PieceIter it(req, first_req, a.B, aj, bj, j);
@@ -743,6 +746,9 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& map_q,
     prm.c_log2 = a.scale * 1.4426950408889634f;
     prm.group_heads = group_heads;
     prm.head_groups = head_groups;
+    // every page the call could read (the capacity of its block tables) within 48 MB
+    const double kv_bound = double(a.B) * a.max_pages * a.P * a.kv_heads * (kDqk * 2);
+    prm.keep_kv = kv_bound <= 48.0 * 1024 * 1024;
     const int grid = a.num_groups * head_groups;
     switch (tc_pad_heads(group_heads)) {
         case 16: return launch_tc<16>(map_q, map_kv, prm, grid, stream);
