@@ -21,7 +21,7 @@ namespace splash {
 
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;
 
 // Optional kernel-boundary trace (compiled in only with -DSPLASH_TRACE): globaltimer
 // stamps of the plan and combine kernels, read back with splash_ktrace_read().
@@ -47,7 +47,7 @@ __device__ int64_t block_inclusive_scan(int64_t v, int64_t* warp_sums) {
     if (lane == 31) warp_sums[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        int64_t s = warp_sums[lane];
+        int64_t s = lane < kPlanThreads / 32 ? warp_sums[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             int64_t n = __shfl_up_sync(0xffffffffu, s, o);
