@@ -283,13 +283,15 @@ class Step:
                                  dtype=inp.pool.dtype, device=device)
         self.src_ids = self.mig.src_ids.to(device)
         self.dst_ids = self.mig.dst_ids.to(device)
+        self.page_bytes = int(inp.pool[0].numel() * inp.pool.element_size())
         self.pattern += f" + {int(round(100 * frac))}% KV-page handoff ({self.src_ids.numel()} pages)"
         if len(self.calls) > 1:
             self.pattern += "; decode calls alternate between two streams, one workspace each"
+            if self.migrate_bytes() <= (64 << 20):
+                self.pattern += "; the (small) migration runs on the second stream alongside the merge"
         self.launches_per_step = 3 * len(self.calls) + (1 if self.merge else 0) + 1
         if not hasattr(self, "ranges"):
             self.ranges = None
-        self.page_bytes = int(inp.pool[0].numel() * inp.pool.element_size())
 
     def call_algorithmic(self, c):
         """(bytes, flops) one decode call must move / do."""
@@ -353,17 +355,28 @@ class Step:
             cur.wait_event(join)
         if decode_events is not None:
             decode_events[1].record()
+        # the handoff's migration does not depend on the merge: a small one runs on the
+        # second stream alongside the merge; a large one would contend with the merge and
+        # the decode tail for SMs and HBM (see the background-handoff measurement), so it
+        # runs after them
+        two = len(self.calls) > 1 and self.migrate_bytes() <= (64 << 20)
+        mig_stream = self.stream_b if two else cur
+        with torch.cuda.stream(mig_stream):
+            if row_events is not None:
+                row_events["kv_migrate"][0].record()
+            self.S.splash_kv_migrate(self.inp.pool, self.pool2, self.src_ids, self.dst_ids)
+            if row_events is not None:
+                row_events["kv_migrate"][1].record()
         if self.merge:
             if row_events is not None:
                 row_events["lse_merge"][0].record()
             self.S.splash_lse_merge(self.po, self.pl, self.out, self.lse)
             if row_events is not None:
                 row_events["lse_merge"][1].record()
-        if row_events is not None:
-            row_events["kv_migrate"][0].record()
-        self.S.splash_kv_migrate(self.inp.pool, self.pool2, self.src_ids, self.dst_ids)
-        if row_events is not None:
-            row_events["kv_migrate"][1].record()
+        if two:
+            done = torch.cuda.Event()
+            done.record(self.stream_b)
+            cur.wait_event(done)
 
     def run_background_handoff(self, side2, max_sms, dec_events, join_event):
         """The step's decode calls on the current stream with at most max_sms SMs, while
