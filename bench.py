@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--reserved-sms", type=int, default=16,
                     help="SMs left to the background page migration in the handoff-overlap "
                          "measurement")
+    ap.add_argument("--call-sms", type=int, default=-1,
+                    help="SM budget of each decode call of a multi-call step (-1: half the "
+                         "SMs when every call fits in one wave, else all; 0: all)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -232,7 +235,7 @@ class Step:
     25%) of the requests' pages into a second pool.
     """
 
-    def __init__(self, w, inp, device, ranges=None):
+    def __init__(self, w, inp, device, ranges=None, call_sms=-1):
         import torch
         from layout_agnostic_paged_gb300 import splash as S
         from layout_agnostic_paged_gb300 import workloads as W
@@ -292,6 +295,35 @@ class Step:
         self.launches_per_step = 3 * len(self.calls) + (1 if self.merge else 0) + 1
         if not hasattr(self, "ranges"):
             self.ranges = None
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        self.call_sms = self.pick_call_sms(sms) if call_sms < 0 else call_sms
+        if self.call_sms:
+            self.pattern += (f"; each call limited to {self.call_sms} of {sms} SMs, so the two "
+                             f"streams' calls run side by side")
+
+    def call_cta_tiles(self, c):
+        """(128-token tiles x 64-head groups) one decode call must process."""
+        hl, hh, lo, hi, _, _ = c
+        i = next(k for k, x in enumerate(self.calls) if x is c)
+        rng = self.ranges[i].cpu().tolist() if self.ranges is not None else None
+        tiles = 0
+        for r, L in enumerate(self.w.ctx_lens):
+            if rng is not None:
+                lo, hi = rng[0][r], rng[1][r]
+            a, b = max(lo, 0), (L if hi < 0 else min(hi, L))
+            if b > a:
+                tiles += (b - 1) // 128 - a // 128 + 1
+        return tiles * -(-(hh - hl) // 64)
+
+    def pick_call_sms(self, sms):
+        """A call whose tiles fill at most one wave of the GPU leaves SMs idle while the
+        other stream's call waits for them; two such calls each get half the SMs and run
+        side by side (two CP ranks sharing one GPU).  Larger calls keep every SM."""
+        if len(self.calls) < 2:
+            return 0
+        if all(self.call_cta_tiles(c) <= sms for c in self.calls):
+            return sms // 2
+        return 0
 
     def call_algorithmic(self, c):
         """(bytes, flops) one decode call must move / do."""
@@ -346,9 +378,9 @@ class Step:
         for k, c in enumerate(self.calls):
             if k % 2:
                 with torch.cuda.stream(self.stream_b):
-                    self.decode(c, q, bt, ctx, ws=self.ws_b)
+                    self.decode(c, q, bt, ctx, max_sms=self.call_sms, ws=self.ws_b)
             else:
-                self.decode(c, q, bt, ctx)
+                self.decode(c, q, bt, ctx, max_sms=self.call_sms)
         if len(self.calls) > 1:
             join = torch.cuda.Event()
             join.record(self.stream_b)
@@ -455,7 +487,8 @@ def run_ours(args, world, rank, local):
         ins.append(W.per_request_ranges(w))
     in_pack, views = pack(ins, device)
     inp.q, inp.block_table, inp.ctx_lens = views[:3]
-    step = Step(w, inp, device, ranges=views[3] if w.per_request_splits else None)
+    step = Step(w, inp, device, ranges=views[3] if w.per_request_splits else None,
+                call_sms=args.call_sms)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     K, Wm = args.steps, args.warmup
 

@@ -25,7 +25,7 @@ constexpr int kTileTokens = 128; // token tile of every decode kernel (the MMA M
 // ---------------------------------------------------------------------------
 struct PlanHeader {
     uint32_t status;       // SPLASH_DEVICE_* bits of the last call
-    int32_t num_groups;    // CTA groups in use: min(G', T); the tile sequence is cut in that many ranges
+    int32_t num_groups;    // CTA groups in use (<= G', <= T); the tile sequence is cut in that many ranges
     int64_t total_tiles;   // T: tiles over all requests
     int32_t num_reqs;
     int32_t heads;         // Hs = head_hi - head_lo

@@ -87,6 +87,9 @@ __device__ __forceinline__ ReqPlan request_span(int L, int64_t tok_lo, int64_t t
     return p;
 }
 
+// Largest tiles-per-group count for which the plan uses fewer CTA groups than it may.
+constexpr int64_t kRegroupMaxTiles = 4;
+
 // Requests whose tile ends the plan keeps in shared memory for the group search;
 // larger batches search the plan in global memory.
 constexpr int kPlanSmemReqs = 8192;
@@ -156,9 +159,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     if (threadIdx.x == kPlanThreads - 1) s_total = incl;
     __syncthreads();
     const int64_t T = s_total;
-    // Never more CTA groups than tiles: every group range is then non-empty, so a
-    // request's pieces are exactly the groups its tiles fall in.
-    const int64_t G = min(int64_t(num_groups), T);
+    // The busiest group gets k = ceil(T / num_groups) tiles whatever the cut.  When k is
+    // small, ceil(T / k) groups keep that critical path while giving every group k or
+    // k - 1 tiles: fewer requests are split (fewer partial rows to merge) and the spare
+    // SMs are free for concurrent work.  For long runs of tiles the extra tile on the
+    // average group costs more than it saves, so every group is used.  G <= T makes
+    // every group range non-empty, so a request's pieces are exactly the groups its
+    // tiles fall in.
+    const int64_t k = T > 0 ? (T + num_groups - 1) / num_groups : 0;
+    const int64_t G = k == 0 ? 0 : k <= kRegroupMaxTiles ? (T + k - 1) / k : min(int64_t(num_groups), T);
 
     // Pass 2: global tile offsets, CTA-group cut and partial-slot counts.
     int64_t my_slots = 0;

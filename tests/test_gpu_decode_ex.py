@@ -145,7 +145,7 @@ def test_bad_row_and_negative_start_are_flagged_and_skipped():
     _check_request(inp, out, lse, 2, 100, -1, "request 2")
 
 
-@pytest.mark.parametrize("max_sms", [1, 7, 16, 100000])
+@pytest.mark.parametrize("max_sms", [1, 7, 16, 34, 80, 100000])
 def test_sm_budget_changes_the_split_not_the_result(max_sms):
     """A decode grid held to max_sms SMs (the rest left to background work) cuts the
     tiles differently but computes the same attention."""
@@ -155,3 +155,13 @@ def test_sm_budget_changes_the_split_not_the_result(max_sms):
     for r in range(len(ctx)):
         _check_request(inp, out, lse, r, 0, -1, f"max_sms={max_sms} request {r}")
     assert S.splash_workspace_status(ws) == 0
+    # the plan's cut: at most ceil(T / groups) tiles on a group; with at most 4 tiles per
+    # group it uses the fewest groups that keep that count, else every group (<= T)
+    hdr = ws[:16].cpu()
+    G = int(hdr[4:8].view(torch.int32)[0])
+    T = int(hdr[8:16].view(torch.int64)[0])
+    assert T == sum(-(-L // 128) for L in ctx)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    groups = max(1, min(sms, max_sms) // 2)      # 128 heads: two head-group CTAs per group
+    k = -(-T // groups)
+    assert G == (-(-T // k) if k <= 4 else min(groups, T)), (G, T, groups)
