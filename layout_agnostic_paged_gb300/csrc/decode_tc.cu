@@ -276,7 +276,6 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
 
     if (threadIdx.x == 0) TRACE(1);
     pdl_wait();     // the plan (and every earlier kernel on the stream) is complete
-    pdl_trigger();  // the combine grid may start launching
     if (threadIdx.x == 0) TRACE(2);
     const int64_t T = hdr->total_tiles;
     const int G = hdr->num_groups;  // groups in use (<= a.num_groups, <= T)
@@ -700,6 +699,9 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
         }
     }
 
+    // only now may the combine grid launch: launched at the start, its waiting CTAs would
+    // hold the SMs that a decode call on another stream needs
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) TRACE(42);

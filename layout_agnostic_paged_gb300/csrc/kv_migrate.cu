@@ -26,7 +26,6 @@ __global__ void __launch_bounds__(kMigThreads) kv_migrate_kernel(
     int chunks_per_page, const int32_t* __restrict__ src_ids,
     const int32_t* __restrict__ dst_ids, int n, int src_np, int dst_np) {
     pdl_wait();
-    pdl_trigger();
     const int64_t items = int64_t(n) * chunks_per_page;
     for (int64_t i = blockIdx.x; i < items; i += gridDim.x) {
         const int pg = int(i / chunks_per_page);

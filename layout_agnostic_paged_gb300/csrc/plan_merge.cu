@@ -306,7 +306,6 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict_
                                                       float* __restrict__ lse) {
     if (threadIdx.x == 0) KTRACE_MIN(3);
     pdl_wait();
-    pdl_trigger();
     if (threadIdx.x == 0) KTRACE_MIN(4);
     if (threadIdx.x == 0) KTRACE_MAX(5);
     const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -338,7 +337,6 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
                                                         float* __restrict__ out,
                                                         float* __restrict__ lse) {
     pdl_wait();
-    pdl_trigger();
     const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (row >= rows) return;
     warp_lse_merge(part_out + row * d_v, rows * d_v, part_lse + row, rows, S, d_v,
