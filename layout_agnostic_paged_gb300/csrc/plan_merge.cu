@@ -237,12 +237,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 // Merge `S` partial rows (out at stride `ostride` floats, lse at stride `lstride`)
 // into one output row; one warp.  Lane s < 32 owns split s's weight (broadcast by
 // shuffles, the lse column read once); lanes cover d_v in float4 steps with the
-// loads of up to 4 splits (16 float4 per lane) in flight.
+// loads of up to 4 splits (16 float4 per lane) in flight.  Splits are added in
+// index order on every path.
 __device__ __forceinline__ void warp_lse_merge(const float* __restrict__ pout, int64_t ostride,
                                                const float* __restrict__ plse, int64_t lstride,
                                                int S, int d_v, float* __restrict__ out,
                                                float* __restrict__ lse) {
     const int lane = threadIdx.x & 31;
+    // For 512-wide rows (one pass) the first four splits' rows are loaded together with
+    // the lse column, so the row loads do not wait for the weights.
+    float4 pre[4][4];
+    const bool one_pass = d_v == 512;
+    if (one_pass) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            if (t < S)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    pre[t][c] = *reinterpret_cast<const float4*>(pout + t * ostride + lane * 4 + c * 128);
+    }
     // up to 32 splits: one load of the lse column, kept in a register for all passes
     const float l0 = (lane < S) ? plse[lane * lstride] : -INFINITY;
     float m = l0;
@@ -262,6 +275,49 @@ __device__ __forceinline__ void warp_lse_merge(const float* __restrict__ pout, i
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     const float inv = 1.0f / wsum;
+    if (one_pass) {
+        const float myw = (lane < S) ? expf(l0 - m) : 0.f;
+        float4 acc[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            if (t < S) {
+                const float w = __shfl_sync(0xffffffffu, myw, t);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    acc[c].x += w * pre[t][c].x;
+                    acc[c].y += w * pre[t][c].y;
+                    acc[c].z += w * pre[t][c].z;
+                    acc[c].w += w * pre[t][c].w;
+                }
+            }
+        }
+        for (int s0 = 0; s0 < S; s0 += 32) {      // splits 4.. in the same order
+            const float w_s = s0 == 0 ? myw
+                                      : ((s0 + lane < S) ? expf(plse[(s0 + lane) * lstride] - m) : 0.f);
+            const int n = min(32, S - s0);
+#pragma unroll 4
+            for (int t = (s0 == 0 ? 4 : 0); t < n; ++t) {
+                const float w = __shfl_sync(0xffffffffu, w_s, t);
+                const float* src = pout + (s0 + t) * ostride + lane * 4;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float4 o = *reinterpret_cast<const float4*>(src + c * 128);
+                    acc[c].x += w * o.x;
+                    acc[c].y += w * o.y;
+                    acc[c].z += w * o.z;
+                    acc[c].w += w * o.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<float4*>(out + lane * 4 + c * 128) =
+                make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv);
+        if (lane == 0) *lse = m + logf(wsum);
+        return;
+    }
     for (int j0 = 0; j0 < d_v; j0 += 512) {       // 512 floats per pass: 4 float4 per lane
         float4 acc[4];
 #pragma unroll
