@@ -29,3 +29,53 @@ def test_bench_module_imports_without_gpu():
     import bench
     assert bench.UNIT == "KV-tokens/s"
     assert len(bench.kernel_source_hash()) == 16
+
+
+def _fake_step(w, calls, ranges=None):
+    """A bench Step holding only what the call-size logic reads (no device buffers)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    st = bench.Step.__new__(bench.Step)
+    st.w, st.calls, st.ranges = w, calls, ranges
+    return st
+
+
+def test_small_two_call_steps_get_half_the_sms():
+    """A multi-call step whose calls each fit in one wave (128-token tiles x 64-head
+    groups <= SMs) gives every call half the SMs; larger calls and single calls keep
+    every SM."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from layout_agnostic_paged_gb300 import workloads as W
+    Step = bench.Step
+    fh = W.full_heads()                       # 16 x 1024 tokens, 128 heads
+    shares = [(0, 128, 0, 512, "out0", None), (0, 128, 512, -1, "out1", None)]
+    st = _fake_step(fh, shares)
+    assert [Step.call_cta_tiles(st, c) for c in shares] == [16 * 4 * 2, 16 * 4 * 2]
+    assert Step.pick_call_sms(st, 152) == 76
+    assert Step.pick_call_sms(st, 100) == 0   # 128 CTA-tiles no longer fit in one wave
+    one = _fake_step(fh, shares[:1])
+    assert Step.pick_call_sms(one, 152) == 0
+    cp = W.cp_long()                          # 8 shares of 8,192 tokens: 2,048 CTA-tiles each
+    cp_calls = [(0, 128, i * 8192, (i + 1) * 8192, f"out{i}", None) for i in range(8)]
+    assert Step.pick_call_sms(_fake_step(cp, cp_calls), 152) == 0
+    hs = W.head_shard()                       # 16-head shards: one head group per call
+    hs_calls = [(i * 16, (i + 1) * 16, 0, -1, f"out{i}", None) for i in range(8)]
+    assert Step.call_cta_tiles(_fake_step(hs, hs_calls), hs_calls[0]) == 128 * 32
+
+
+def test_per_request_ranges_count_their_own_tiles():
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch
+    from layout_agnostic_paged_gb300 import workloads as W
+    w = W.Workload("ragged shares", (300, 1000, 0), 128, 64, seed=1, token_splits=2,
+                   per_request_splits=True)
+    calls = [(0, 128, 0, -1, "out0", None), (0, 128, 0, -1, "out1", None)]
+    rng = W.per_request_ranges(w)             # share i of request r: [L_r i / 2, L_r (i + 1) / 2)
+    st = _fake_step(w, calls, rng)
+    # share 0: [0,150) -> tiles 0-1, [0,500) -> tiles 0-3, empty;
+    # share 1: [150,300) -> tiles 1-2, [500,1000) -> tiles 3-7, empty
+    assert bench.Step.call_cta_tiles(st, calls[0]) == (2 + 4) * 2
+    assert bench.Step.call_cta_tiles(st, calls[1]) == (2 + 5) * 2
+    assert torch.equal(rng[0, 1], torch.tensor([150, 500, 0], dtype=torch.int32))
