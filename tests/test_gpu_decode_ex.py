@@ -165,3 +165,31 @@ def test_sm_budget_changes_the_split_not_the_result(max_sms):
     groups = max(1, min(sms, max_sms) // 2)      # 128 heads: two head-group CTAs per group
     k = -(-T // groups)
     assert G == (-(-T // k) if k <= 4 else min(groups, T)), (G, T, groups)
+
+
+def test_concurrent_share_calls_on_two_streams_with_half_the_sms():
+    """Two CP share calls issued on two streams at once, each held to half the SMs and
+    with its own workspace (the benchmark's pattern for small steps), then merged:
+    the same result as the unsplit oracle."""
+    ctx = [1024] * 6 + [700, 129]
+    inp = W.make_decode_inputs(ctx, 128, 64, seed=52, device=DEV)
+    B = len(ctx)
+    half = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    po = torch.full((2, B, 128, 512), float("nan"), device=DEV)
+    pl = torch.full((2, B, 128), float("nan"), device=DEV)
+    wss = [S.decode_workspace(inp.q, inp.pool, inp.block_table, W.MLA_SCALE) for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for i, (lo, hi) in enumerate([(0, 512), (512, -1)]):
+        with torch.cuda.stream(streams[i]):
+            S.splash_decode_attn_ex(inp.q, inp.pool, inp.block_table, inp.ctx_lens, 0, 128, lo, hi,
+                                    po[i], pl[i], wss[i], W.MLA_SCALE, max_sms=half)
+    torch.cuda.synchronize()
+    mo = torch.empty(B, 128, 512, device=DEV)
+    ml = torch.empty(B, 128, device=DEV)
+    S.splash_lse_merge(po, pl, mo, ml)
+    torch.cuda.synchronize()
+    for ws in wss:
+        assert S.splash_workspace_status(ws) == 0
+    for r in range(B):
+        _check_request(inp, mo, ml, r, 0, -1, f"two-stream shares, request {r}")
