@@ -79,3 +79,51 @@ def test_per_request_ranges_count_their_own_tiles():
     assert bench.Step.call_cta_tiles(st, calls[0]) == (2 + 4) * 2
     assert bench.Step.call_cta_tiles(st, calls[1]) == (2 + 5) * 2
     assert torch.equal(rng[0, 1], torch.tensor([150, 500, 0], dtype=torch.int32))
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _reduce_worker(rank, world, port, results):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        sys.path.insert(0, ROOT)
+        import bench
+        bench.barrier(world)
+        results[rank] = (bench.max_over_ranks(rank + 1.5, world, "cpu"),
+                         bench.sum_over_ranks(rank + 1.5, world, "cpu"))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_timing_reductions_over_two_gloo_ranks():
+    """The benchmark's cross-rank reductions (max of the times, sum of the tokens) and
+    barrier, on two CPU ranks over gloo."""
+    import torch.multiprocessing as mp
+    world = 2
+    with mp.Manager() as m:
+        results = m.dict()
+        mp.spawn(_reduce_worker, args=(world, _free_port(), results), nprocs=world, join=True)
+        got = dict(results)
+    assert got == {0: (2.5, 4.0), 1: (2.5, 4.0)}
+
+
+def test_reference_arm_prints_once_under_two_ranks():
+    """Launched as two ranks, the reference arm runs on rank 0 only: one JSON line, and
+    every rank exits 0."""
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes", "1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1", "--master-port",
+                        str(_free_port()), os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "1", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
