@@ -244,3 +244,23 @@ def test_ragged_handoff_workload_sampled():
     r0 = 0
     ro, rl = oracle_rows(inp2, w.scale, r0, 120, 128)
     assert_attn_close(o2[r0, 120:].cpu(), ro, l2[r0, 120:].cpu(), rl, "migrated vs oracle")
+
+
+def test_batch_beyond_the_plans_shared_memory_search():
+    """More requests (9,000) than the plan keeps tile ends for in shared memory (8,192):
+    the group search then reads the plan from global memory.  Short ragged contexts,
+    some empty; sampled requests against the oracle, and every output finite."""
+    rng = np.random.default_rng(60)
+    ctx = [int(x) for x in rng.integers(0, 400, size=9000)]
+    inp = W.make_decode_inputs(ctx, 16, 64, seed=60, device=DEV)
+    out, lse, ws = gpu_decode(inp, W.MLA_SCALE)
+    torch.cuda.synchronize()
+    assert S.splash_workspace_status(ws) == 0
+    nonempty = [r for r, L in enumerate(ctx) if L > 0]
+    assert torch.isfinite(out[nonempty]).all() and torch.isfinite(lse[nonempty]).all()
+    empty = [r for r, L in enumerate(ctx) if L == 0]
+    assert empty and (out[empty] == 0).all() and torch.isneginf(lse[empty]).all()
+    for r in [nonempty[0], 4095, 8191, 8192, 8193, nonempty[-1]] + list(rng.choice(nonempty, 6)):
+        r = int(r)
+        ro, rl = oracle_rows(inp, W.MLA_SCALE, r, 0, 16)
+        assert_attn_close(out[r].cpu(), ro, lse[r].cpu(), rl, f"request {r} of 9000")
