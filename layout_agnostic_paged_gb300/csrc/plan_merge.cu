@@ -2,9 +2,10 @@
 // and the public log-sum-exp merge (K4).
 //
 // The plan balances ragged requests across the persistent decode grid: all
-// requests' 128-token tiles are concatenated and cut into G' equal ranges, one
-// per CTA group; a request cut across several groups yields one partial per
-// group, combined by K3 with the same log-sum-exp merge K4 exposes.  The cut
+// requests' 128-token tiles are concatenated and cut into at most G' near-equal
+// ranges, one per CTA group (fewer when a range would hold only a few tiles); a
+// request cut across several groups yields one partial per group, combined by K3
+// with the same log-sum-exp merge K4 exposes.  The cut
 // depends only on the context lengths and the token range, never on physical
 // page ids, so results are identical under any page permutation.
 //
