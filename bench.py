@@ -7,7 +7,9 @@ the full-heads workload: B=16, ctx 1,024, 128 query heads, one shared 576-wide
 latent KV head, page 64, shuffled page ids):
   * CP layout: two token-share decode calls ([0, L/2) and [L/2, L)), each = split
     plan + tensor-core decode + split combine, producing partial out + LSE; the
-    calls are independent and alternate between two streams, one workspace each;
+    calls are independent and alternate between two streams, one workspace each,
+    and calls that fit in one wave of the GPU are held to half the SMs each so that
+    the two run side by side (--call-sms);
   * splash_lse_merge of the two shares into the final out / LSE;
   * a layout handoff: splash_kv_migrate of 25% of the requests' pages into a
     second block pool (the migrated requests' block-table rows are prepared once;
