@@ -264,3 +264,26 @@ def test_batch_beyond_the_plans_shared_memory_search():
         r = int(r)
         ro, rl = oracle_rows(inp, W.MLA_SCALE, r, 0, 16)
         assert_attn_close(out[r].cpu(), ro, lse[r].cpu(), rl, f"request {r} of 9000")
+
+
+@pytest.mark.parametrize("name", ["full_heads", "tiny"])
+def test_benchmark_step_matches_oracle(name):
+    """The step the benchmark times, in its own launch configuration (two share calls
+    on two streams, each on half the SMs, then the merge and the handoff's page
+    migration), against the unsplit fp64 oracle and bit-exact pages."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    w = W.ALL[name]()
+    inp = W.make_workload_inputs(w, device=DEV)
+    step = bench.Step(w, inp, DEV)
+    assert step.call_sms == torch.cuda.get_device_properties(0).multi_processor_count // 2
+    step.run()
+    torch.cuda.synchronize()
+    assert S.splash_workspace_status(step.ws) == 0 and S.splash_workspace_status(step.ws_b) == 0
+    ro, rl = oracle_full(inp, w.scale)
+    assert_attn_close(step.out.cpu(), ro, step.lse.cpu(), rl, f"{name} benchmark step")
+    src = inp.pool.index_select(0, step.src_ids.long())
+    dst = step.pool2.index_select(0, step.dst_ids.long())
+    assert torch.equal(src.view(torch.int16), dst.view(torch.int16))
