@@ -21,7 +21,9 @@
 //   the last    (latent column blocks 2j, 2j+1) and the 16 KB rope block, each page
 //   two warps   fetched through the block table (2D tiled loads, 128-byte swizzle);
 //               the boxes are dealt round-robin to the three warps
-//   warp 1      TMEM allocation and the single MMA-issuing thread
+//   warp 1      TMEM allocation; its lane 0 alone walks the schedule and issues every
+//               MMA (no warp-wide votes or syncs on the path from a landed tile to
+//               its MMAs)
 //   warps 2-5   softmax (S^T from TMEM -> P^T bf16 into the rope slot), zeroing of
 //   (6-9)       V rows past the context (poisoned tails never reach the tensor
 //               core), O rescale, and the epilogue (O^T / l -> out or a partial)
@@ -376,8 +378,9 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // The whole warp walks the schedule; lane 0 issues every tcgen05 instruction.
-        if (aj < bj) {
+        // Lane 0 alone walks the schedule and issues every tcgen05 instruction (the
+        // other lanes go straight to the teardown barrier).
+        if (lane == 0 && aj < bj) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, NPAD, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, NPAD, true, true);
             const uint32_t s_tmem = tmem + C::kSCol;
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
             ReqPlan p;
             bool ok = true;
             while (ok && it.next(pc, p)) {
-                if (!warp_wait(q_full, qph, abort_flag, status)) { ok = false; break; }
+                if (!mbar_wait(q_full, qph, abort_flag, status)) { ok = false; break; }
                 qph ^= 1;
                 int ttr = -kTraceTile0;
                 for (int t = pc.t_lo; t < pc.t_hi; ++t) {
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                     if (lane == 0 && unsigned(ttr) < 3u) TRACE(13 + ttr * 5);
                     // S^T = K_tile . Q^T over the 512 latent dims (pairs) ...
                     for (int jj = 0; jj < 4; ++jj) {
-                        if (!warp_wait(&pair_full[ps], pph, abort_flag, status)) { ok = false; break; }
+                        if (!mbar_wait(&pair_full[ps], pph, abort_flag, status)) { ok = false; break; }
                         if (lane == 0 && ttr == 1) TRACE(51 + jj);
                         tc_fence_after();
                         if (lane == 0) {
@@ -419,12 +422,11 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                                                 db_s + ((c2 * NPAD * 128 + k4 * 32) >> 4), idesc_qk,
                                                 (jj | c2 | k4) != 0);
                         }
-                        __syncwarp();
-                        if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
+                            if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
                     }
                     if (!ok) break;
                     // ... and the 64 rope dims
-                    if (!warp_wait(&rope_full[rs], rph, abort_flag, status)) { ok = false; break; }
+                    if (!mbar_wait(&rope_full[rs], rph, abort_flag, status)) { ok = false; break; }
                     if (lane == 0 && unsigned(ttr) < 3u) TRACE(14 + ttr * 5);
                     tc_fence_after();
                     if (lane == 0) {
@@ -437,13 +439,12 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                         if (last) tc_commit(q_empty);
                         if (unsigned(ttr) < 3u) TRACE(15 + ttr * 5);
                     }
-                    __syncwarp();
                     // O^T += V^T . P^T once the softmax has written P^T into the rope slot
-                    if (!warp_wait(p_full, pfph, abort_flag, status)) { ok = false; break; }
+                    if (!mbar_wait(p_full, pfph, abort_flag, status)) { ok = false; break; }
                     pfph ^= 1;
                     if (lane == 0 && unsigned(ttr) < 3u) TRACE(16 + ttr * 5);
                     if (first) {
-                        if (!warp_wait(o_free, ofph ^ 1, abort_flag, status)) { ok = false; break; }
+                        if (!mbar_wait(o_free, ofph ^ 1, abort_flag, status)) { ok = false; break; }
                         ofph ^= 1;
                     }
                     tc_fence_after();
@@ -471,18 +472,16 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                         if (last) tc_commit(o_full);
                         if (unsigned(ttr) < 3u) TRACE(17 + ttr * 5);
                     }
-                    __syncwarp();
                     ++ttr;
                     if (++rs == C::kRopes) { rs = 0; rph ^= 1; }
                 }
             }
             // drain: every MMA issued so far has completed before TMEM is released
-            if (lane == 0) tc_commit(drain);
-            __syncwarp();
+            tc_commit(drain);
             volatile int never = 0;
             mbar_wait(drain, 0, &never, status);
-            __syncwarp();
         }
+        __syncwarp();   // warp 1 reconverges before the teardown barrier and dealloc
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         // SWG softmax warpgroups; group wg owns heads [hw0, hw0 + HW) of the head group
