@@ -288,7 +288,9 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
         // ------------------------------------------------------------ TMA producers
         // kProducerWarps warps walk the same schedule (each whole warp, so it stays
         // converged); load slot k of a tile (pairs 0-3, then the rope block) and Q box k
-        // belong to producer warp k % kProducerWarps, whose lanes issue them.
+        // belong to producer warp k % kProducerWarps, whose lanes issue them.  A box may
+        // complete before its slot's expect-tx (transaction counts may go negative while
+        // the expect-tx arrival is pending), so no warp sync separates the two.
         const int pw = warp == 0 ? 0 : warp - C::kFirstExtraProducer + 1;
         if (aj < bj) {
             // a small cache stays in L2 for the next kernels (the sibling head group, a
@@ -344,7 +346,6 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                                 mbar_arrive_expect_tx(&pair_full[ps], 2 * blk_bytes);
                                 if (ttr == 1) TRACE(55 + jj);
                             }
-                            __syncwarp();
                             uint8_t* slot = sPair + ps * kPairBytes;
                             if (my_pid >= 0)
                                 for (int c2 = 0; c2 < 2; ++c2)
@@ -352,7 +353,6 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                                         tma_load_2d(slot + c2 * kColBlockBytes + lane * P * 128, &map_kv,
                                                     &pair_full[ps], (2 * jj + c2) * 64,
                                                     (my_pid * a.kv_heads + kvh) * P, pol_kv);
-                            __syncwarp();
                         }
                         if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
                     }
@@ -363,11 +363,9 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                         if (!warp_wait(&rope_empty[rs], rph ^ 1, abort_flag, status)) { ok = false; break; }
                         if (lane == 0 && g0 % kProducerWarps == pw)
                             mbar_arrive_expect_tx(&rope_full[rs], blk_bytes);
-                        __syncwarp();
                         if (my_pid >= 0 && (g0 + lane) % kProducerWarps == pw)
                             tma_load_2d(sRope + rs * kColBlockBytes + lane * P * 128, &map_kv,
                                         &rope_full[rs], 8 * 64, (my_pid * a.kv_heads + kvh) * P, pol_kv);
-                        __syncwarp();
                         if (pw == g0 % kProducerWarps && lane == 0 && unsigned(ttr) < 3u)
                             TRACE(6 + ttr * 3);
                     }
