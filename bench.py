@@ -2,27 +2,30 @@
 """Benchmark of the paged MLA decode hot path on GB300: KV-tokens/s, with the
 decode kernel's roofline fraction and the fp64 CPU oracle as a baseline.
 
-One step = one pass of every hot-path row over one synthetic batch (by default
-the full-heads workload: B=16, ctx 1,024, 128 query heads, one shared 576-wide
-latent KV head, page 64, shuffled page ids):
-  * CP layout: two token-share decode calls ([0, L/2) and [L/2, L)), each = split
-    plan + tensor-core decode + split combine, producing partial out + LSE; the
-    calls are independent and alternate between two streams, one workspace each,
-    and calls that fit in one wave of the GPU are held to half the SMs each so that
-    the two run side by side (--call-sms);
-  * splash_lse_merge of the two shares into the final out / LSE;
-  * a layout handoff: splash_kv_migrate of 25% of the requests' pages into a
-    second block pool (the migrated requests' block-table rows are prepared once;
-    switching tables is a pointer swap, not a kernel).
-value = KV tokens of the batch / step time (each KV token is read once per step).
+One step = one pass of the workload's hot-path rows over one synthetic batch
+(step_pattern).  The default workload is the largest single-GPU configuration,
+the ragged mixed batch with a layout handoff: 256 requests with log-uniform
+contexts of 512..131,072 tokens, 128 query heads over one shared 576-wide latent
+KV head, page 64, shuffled page ids.  Its step is
+  * one decode call over the whole batch (split plan + tcgen05 decode + combine);
+  * the handoff: splash_kv_migrate of a seeded 25% of the requests' pages into a
+    second block pool at fresh page ids (their block-table rows are rewritten on
+    the host, once: an input of the step);
+  * the decode rerun as two calls, each owning its requests as storage rows of the
+    same batch: the remaining requests on pool 1 and the moved ones on pool 2.
+Other workloads (--workload): tiny and full_heads (one call), cp_long (8 token
+shares + splash_lse_merge), head_shard (8 calls of 16 heads), ragged_cp and gqa.
+value = KV tokens decoded for every query head per step (the ragged step decodes
+the batch twice) / step time.
 
 Timing: W untimed warm-up steps, then K timed steps; before every step a 512 MB
 buffer is written to flush the 129 MB L2 (outside the timed events); each step
 is one CUDA graph replay bracketed by CUDA events on the launching stream and the
 K step times are summed; ranks meet at a barrier (+ synchronize) before and after
 and the max over ranks is reported.  A second pass of instrumented graphs gives
-the per-row breakdown, and a third the decode calls with a background page
-migration.  `--impl reference` times the fp64 C oracle instead.
+the per-phase breakdown, and a third the first decode phase with a background
+page migration.  `--impl reference` times the fp64 C oracle instead, running the
+same step pattern over a bounded sample of the requests.
 """
 from __future__ import annotations
 
@@ -37,6 +40,7 @@ import subprocess
 import sys
 import tempfile
 import time
+from dataclasses import dataclass
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -52,13 +56,13 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="full_heads",
-                    help="tiny | full_heads | cp_long | head_shard | ragged_handoff")
+    ap.add_argument("--workload", default="ragged_handoff",
+                    help="ragged_handoff | tiny | full_heads | cp_long | head_shard | ragged_cp | gqa")
     ap.add_argument("--reserved-sms", type=int, default=16,
                     help="SMs left to the background page migration in the handoff-overlap "
                          "measurement")
     ap.add_argument("--call-sms", type=int, default=-1,
-                    help="SM budget of each decode call of a multi-call step (-1: half the "
+                    help="SM budget of each decode call of a multi-call phase (-1: half the "
                          "SMs when every call fits in one wave, else all; 0: all)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -225,218 +229,340 @@ def sum_over_ranks(x: float, world: int, device) -> float:
 
 # ----------------------------------------------------------------------------- the step
 
+@dataclass
+class CallSpec:
+    """One decode call of a step: the ownership slice it computes and where it writes.
+
+    rows: the requests (storage rows) the call owns, None for the whole batch;
+    pool: "pool1" (the batch's pool) or "pool2" (the handoff's destination pool);
+    share: index of the per-request token share (None: the scalar tok_lo / tok_hi);
+    out: "out" (the step's result), "pre" (the output before the handoff) or "part<i>"
+    (CP partial i, merged afterwards)."""
+    head_lo: int
+    head_hi: int
+    tok_lo: int = 0
+    tok_hi: int = -1
+    rows: tuple | None = None
+    pool: str = "pool1"
+    share: int | None = None
+    out: str = "out"
+
+
+def step_pattern(w, moved=None):
+    """The phases of one step of workload w, in order: ("decode", [CallSpec, ...]) (the
+    calls of a phase are independent), ("merge", n) or ("migrate",).
+
+      * TP / DOP head shards (head_shards > 1): one call per head shard;
+      * ragged + handoff (migrate_frac > 0): one call over the batch, the migration of
+        the moved requests' pages to the second pool, then the decode rerun as two calls
+        (the remaining requests on pool 1, the moved ones on pool 2), each owning its
+        requests as storage rows of the same batch;
+      * CP (token_splits > 1): one call per token share, then the merge of the shares;
+      * otherwise one call over the batch.
+    moved: the requests the handoff moves (required when migrate_frac > 0)."""
+    B, H = w.batch, w.num_heads
+    if w.head_shards > 1:
+        hs = H // w.head_shards
+        return [("decode", [CallSpec(i * hs, (i + 1) * hs) for i in range(w.head_shards)])]
+    if w.migrate_frac > 0:
+        mv = set(moved)
+        keep = tuple(r for r in range(B) if r not in mv)
+        return [("decode", [CallSpec(0, H, out="pre")]), ("migrate",),
+                ("decode", [CallSpec(0, H, rows=keep, pool="pool1"),
+                            CallSpec(0, H, rows=tuple(sorted(mv)), pool="pool2")])]
+    if w.token_splits > 1:
+        n = w.token_splits
+        if w.per_request_splits:
+            calls = [CallSpec(0, H, share=i, out=f"part{i}") for i in range(n)]
+        else:
+            span = -(-max(w.ctx_lens) // n)
+            calls = [CallSpec(0, H, i * span, (i + 1) * span if i + 1 < n else -1, out=f"part{i}")
+                     for i in range(n)]
+        return [("decode", calls), ("merge", n)]
+    return [("decode", [CallSpec(0, H)])]
+
+
+def describe_pattern(w, phases):
+    parts = []
+    for ph in phases:
+        if ph[0] == "decode":
+            cs = ph[1]
+            if len(cs) == 1 and cs[0].rows is None:
+                parts.append("one decode call over the batch"
+                             + ("" if cs[0].out != "pre" else " (before the handoff)"))
+            elif w.head_shards > 1:
+                parts.append(f"{len(cs)} head-shard calls of {cs[0].head_hi - cs[0].head_lo} heads")
+            elif cs[0].rows is not None:
+                parts.append(f"decode rerun as {len(cs)} calls owning request subsets in place "
+                             f"({', '.join(f'{len(c.rows)} on {c.pool}' for c in cs)})")
+            else:
+                kind = "per-request token-share" if cs[0].share is not None else "token-share"
+                parts.append(f"{len(cs)} CP {kind} calls")
+        elif ph[0] == "merge":
+            parts.append(f"splash_lse_merge of {ph[1]} shares")
+        else:
+            parts.append(f"splash_kv_migrate of {int(round(100 * w.migrate_frac))}% of the "
+                         f"requests' pages to a second pool")
+    return " -> ".join(parts)
+
+
+def call_tokens_pages(w, c, ranges=None):
+    """(KV tokens, pages) call c reads (ranges: the per-request share bounds, [n][2][B])."""
+    toks = pages = 0
+    P = w.page_size
+    rows = range(w.batch) if c.rows is None else c.rows
+    for r in rows:
+        L = w.ctx_lens[r]
+        if c.share is not None:
+            lo, hi = int(ranges[c.share][0][r]), int(ranges[c.share][1][r])
+        else:
+            lo, hi = c.tok_lo, c.tok_hi
+        a, b = max(lo, 0), (L if hi < 0 else min(hi, L))
+        if b > a:
+            toks += b - a
+            pages += (b - 1) // P - a // P + 1
+    return toks, pages
+
+
+def call_cta_tiles(w, c, ranges=None):
+    """(128-token tiles x 64-head groups) one decode call must process."""
+    tiles = 0
+    rows = range(w.batch) if c.rows is None else c.rows
+    for r in rows:
+        L = w.ctx_lens[r]
+        if c.share is not None:
+            lo, hi = int(ranges[c.share][0][r]), int(ranges[c.share][1][r])
+        else:
+            lo, hi = c.tok_lo, c.tok_hi
+        a, b = max(lo, 0), (L if hi < 0 else min(hi, L))
+        if b > a:
+            tiles += (b - 1) // 128 - a // 128 + 1
+    return tiles * -(-(c.head_hi - c.head_lo) // 64)
+
+
+def pick_call_sms(w, calls, sms, ranges=None):
+    """A phase of several calls whose tiles each fill at most one wave of the GPU would
+    leave SMs idle while the other stream's call waits for them; such calls each get
+    half the SMs and run side by side (two ranks sharing one GPU).  Larger calls, and a
+    phase of one call, keep every SM."""
+    if len(calls) < 2:
+        return 0
+    if all(call_cta_tiles(w, c, ranges) <= sms for c in calls):
+        return sms // 2
+    return 0
+
+
+def algorithmic(Hs, tokens_in_call, rows, pages, kv_heads_read=1):
+    """Bytes and flops one decode call must move / do: every KV token once (576 bf16
+    per KV head the call reads), q rows (576 bf16), fp32 out rows + lse, 4 bytes per
+    page id."""
+    bytes_ = (tokens_in_call * 576 * 2 * kv_heads_read + rows * 576 * 2 + rows * (512 * 4 + 4)
+              + pages * 4)
+    flops = 2.0 * tokens_in_call * Hs * (576 + 512)
+    return bytes_, flops
+
+
+def call_algorithmic(w, c, ranges=None):
+    toks, pages = call_tokens_pages(w, c, ranges)
+    Hs = c.head_hi - c.head_lo
+    nreq = w.batch if c.rows is None else len(c.rows)
+    Hkv = w.num_kv_heads
+    kv_read = 1 if Hkv == 1 else len({h // (w.num_heads // Hkv) for h in range(c.head_lo, c.head_hi)})
+    return algorithmic(Hs, toks, nreq * Hs, pages, kv_read)
+
+
+def decoded_tokens(w, phases, ranges=None):
+    """KV tokens a step decodes for every query head: the sum over its calls of the
+    call's tokens times the share of the heads it covers."""
+    t = 0.0
+    for ph in phases:
+        if ph[0] == "decode":
+            for c in ph[1]:
+                t += call_tokens_pages(w, c, ranges)[0] * (c.head_hi - c.head_lo) / w.num_heads
+    return int(round(t))
+
+
+def workload_config(w, phases, world):
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": w.name, "global_batch": w.batch * world, "seq_len": max(w.ctx_lens),
+            "heads": w.num_heads, "page_size": w.page_size,
+            "kv_tokens_per_rank": w.kv_tokens,
+            "decoded_kv_tokens_per_step_per_rank": decoded_tokens(
+                w, phases, per_request_ranges_or_none(w)),
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "step": describe_pattern(w, phases),
+            "l2": "inputs larger than L2 where the workload's cache is; a 512 MB flush write "
+                  "before every timed step in every case"}
+
+
+def per_request_ranges_or_none(w):
+    if not w.per_request_splits:
+        return None
+    from layout_agnostic_paged_gb300 import workloads as W
+    return W.per_request_ranges(w).tolist()
+
+
 class Step:
-    """Buffers and calls of one step over one batch (see the module docstring).
+    """Device buffers and calls of one step over one batch (see step_pattern)."""
 
-    The step pattern follows the workload's layout:
-      * CP (tiny, full_heads, cp_long): max(2, token_splits) token-share calls, then
-        splash_lse_merge of the shares;
-      * TP / DOP head shards (head_shard): one call per head shard, rows concatenate;
-      * DP-attention / DOP whole requests (ragged_handoff): one call over the batch.
-    Every pattern ends with the handoff: splash_kv_migrate of migrate_frac (default
-    25%) of the requests' pages into a second pool.
-    """
-
-    def __init__(self, w, inp, device, ranges=None, call_sms=-1):
+    def __init__(self, w, inp, device, call_sms=-1, migration=None):
         import torch
         from layout_agnostic_paged_gb300 import splash as S
         from layout_agnostic_paged_gb300 import workloads as W
-        self.S = S
-        self.w = w
-        self.inp = inp
+        self.S, self.w, self.inp = S, w, inp
         B, H = w.batch, w.num_heads
         self.B, self.H = B, H
-        # out and lse share one buffer so that the end-to-end leg reads them back at once
+        self.mig = None
+        if w.migrate_frac > 0:
+            self.mig = migration or W.make_migration(inp, w.migrate_frac, seed=w.seed)
+        self.phases = step_pattern(w, self.mig.requests if self.mig else None)
+        self.pattern = describe_pattern(w, self.phases)
+        # host inputs that the end-to-end leg copies in every step: q, block table(s),
+        # context lengths, request rows, per-request ranges -- packed in one buffer
+        ins = {"q": inp.q, "bt1": inp.block_table, "ctx": inp.ctx_lens}
+        if self.mig is not None:
+            bt2 = torch.full(tuple(inp.block_table.shape), -1, dtype=torch.int32)
+            bt2[torch.tensor(self.mig.requests, dtype=torch.long)] = self.mig.new_block_table
+            ins["bt2"] = bt2
+        self.rows_key = {}
+        for ph in self.phases:
+            if ph[0] == "decode":
+                for k, c in enumerate(ph[1]):
+                    if c.rows is not None:
+                        key = f"rows_{c.pool}"
+                        ins[key] = torch.tensor(c.rows, dtype=torch.int32)
+                        self.rows_key[id(c)] = key
+        self.ranges_host = per_request_ranges_or_none(w)
+        if self.ranges_host is not None:
+            ins["ranges"] = W.per_request_ranges(w)
+        self.in_pack, views = pack(list(ins.values()), device)
+        self.dev = dict(zip(ins.keys(), views))
+        inp.q, inp.block_table, inp.ctx_lens = self.dev["q"], self.dev["bt1"], self.dev["ctx"]
+        # outputs: the step's result (read back by the end-to-end leg) and scratch outputs
         self.out_pack, (self.out, self.lse) = pack(
             [torch.empty(B, H, 512), torch.empty(B, H)], device)
-        self.calls = []          # (head_lo, head_hi, tok_lo, tok_hi, out, lse)
-        self.merge = False
-        if w.head_shards > 1:
-            hs = H // w.head_shards
-            for i in range(w.head_shards):
-                self.calls.append((i * hs, (i + 1) * hs, 0, -1, self.out, self.lse))
-            self.pattern = f"{w.head_shards} head-shard calls of {hs} heads"
-        elif w.migrate_frac > 0 and w.token_splits == 1:
-            self.calls.append((0, H, 0, -1, self.out, self.lse))
-            self.pattern = "one whole-request call over the batch"
-        else:
-            n = max(2, w.token_splits)
-            L = max(w.ctx_lens)
-            span = -(-L // n)
-            self.po = torch.empty(n, B, H, 512, device=device)
-            self.pl = torch.empty(n, B, H, device=device)
-            for i in range(n):
-                self.calls.append((0, H, i * span, (i + 1) * span if i + 1 < n else -1,
-                                   self.po[i], self.pl[i]))
-            self.merge = True
-            self.pattern = f"{n} CP token-share calls + LSE merge"
-            if w.per_request_splits:
-                # share i of request r: [L_r i / n, L_r (i + 1) / n), per-request ranges
-                self.ranges = ranges if ranges is not None else W.per_request_ranges(w).to(device)
-                self.pattern = (f"{n} CP calls with per-request token shares "
-                                f"(splash_decode_attn_ex) + LSE merge")
-        hs0 = self.calls[0][1] - self.calls[0][0]
-        self.ws = S.decode_workspace(inp.q, inp.pool, inp.block_table, w.scale, 0, hs0)
-        # the step's decode calls are independent: odd calls go to a second stream with a
-        # workspace of their own, so one call's tail overlaps the next call's start
-        self.ws_b = (S.decode_workspace(inp.q, inp.pool, inp.block_table, w.scale, 0, hs0)
-                     if len(self.calls) > 1 else None)
+        self.outs = {"out": (self.out, self.lse)}
+        n_parts = max([ph[1] for ph in self.phases if ph[0] == "merge"], default=0)
+        if n_parts:
+            self.po = torch.empty(n_parts, B, H, 512, device=device)
+            self.pl = torch.empty(n_parts, B, H, device=device)
+            for i in range(n_parts):
+                self.outs[f"part{i}"] = (self.po[i], self.pl[i])
+        if any(c.out == "pre" for ph in self.phases if ph[0] == "decode" for c in ph[1]):
+            self.outs["pre"] = (torch.empty(B, H, 512, device=device),
+                                torch.empty(B, H, device=device))
+        self.pool2 = None
+        if self.mig is not None:
+            self.pool2 = torch.empty((self.mig.dst_num_pages,) + tuple(inp.pool.shape[1:]),
+                                     dtype=inp.pool.dtype, device=device)
+            self.src_ids = self.mig.src_ids.to(device)
+            self.dst_ids = self.mig.dst_ids.to(device)
+            self.page_bytes = int(inp.pool[0].numel() * inp.pool.element_size())
+        # calls of a phase alternate between the current stream and a second one, each
+        # with its own workspace (sized for the largest call it runs)
         self.stream_b = torch.cuda.Stream(device)
-        frac = w.migrate_frac if w.migrate_frac > 0 else 0.25
-        self.mig = W.make_migration(inp, frac, seed=w.seed)
-        self.pool2 = torch.empty((self.mig.dst_num_pages,) + tuple(inp.pool.shape[1:]),
-                                 dtype=inp.pool.dtype, device=device)
-        self.src_ids = self.mig.src_ids.to(device)
-        self.dst_ids = self.mig.dst_ids.to(device)
-        self.page_bytes = int(inp.pool[0].numel() * inp.pool.element_size())
-        self.pattern += f" + {int(round(100 * frac))}% KV-page handoff ({self.src_ids.numel()} pages)"
-        if len(self.calls) > 1:
-            self.pattern += "; decode calls alternate between two streams, one workspace each"
-            if self.migrate_bytes() <= (64 << 20):
-                self.pattern += "; the (small) migration runs on the second stream alongside the merge"
-        self.launches_per_step = 3 * len(self.calls) + (1 if self.merge else 0) + 1
-        if not hasattr(self, "ranges"):
-            self.ranges = None
+        need = [0, 0]
+        for ph in self.phases:
+            if ph[0] == "decode":
+                for k, c in enumerate(ph[1]):
+                    nreq = B if c.rows is None else len(c.rows)
+                    ws = S.decode_workspace(inp.q, inp.pool, inp.block_table, w.scale, c.head_lo,
+                                            c.head_hi, num_reqs=nreq)
+                    need[k % 2] = max(need[k % 2], ws.numel())
+                    del ws
+        self.ws = torch.empty(need[0], dtype=torch.uint8, device=device)
+        self.ws_b = torch.empty(need[1], dtype=torch.uint8, device=device) if need[1] else None
         sms = torch.cuda.get_device_properties(device).multi_processor_count
-        self.call_sms = self.pick_call_sms(sms) if call_sms < 0 else call_sms
-        if self.call_sms:
-            self.pattern += (f"; each call limited to {self.call_sms} of {sms} SMs, so the two "
-                             f"streams' calls run side by side")
+        self.sms = sms
+        self.call_sms = {}
+        for ph in self.phases:
+            if ph[0] == "decode":
+                s = pick_call_sms(w, ph[1], sms, self.ranges_host) if call_sms < 0 else call_sms
+                for c in ph[1]:
+                    self.call_sms[id(c)] = s
+        self.launches_per_step = sum(3 * len(ph[1]) if ph[0] == "decode" else 1
+                                     for ph in self.phases)
 
-    def call_cta_tiles(self, c):
-        """(128-token tiles x 64-head groups) one decode call must process."""
-        hl, hh, lo, hi, _, _ = c
-        i = next(k for k, x in enumerate(self.calls) if x is c)
-        rng = self.ranges[i].cpu().tolist() if self.ranges is not None else None
-        tiles = 0
-        for r, L in enumerate(self.w.ctx_lens):
-            if rng is not None:
-                lo, hi = rng[0][r], rng[1][r]
-            a, b = max(lo, 0), (L if hi < 0 else min(hi, L))
-            if b > a:
-                tiles += (b - 1) // 128 - a // 128 + 1
-        return tiles * -(-(hh - hl) // 64)
+    def decode_calls(self):
+        return [c for ph in self.phases if ph[0] == "decode" for c in ph[1]]
 
-    def pick_call_sms(self, sms):
-        """A call whose tiles fill at most one wave of the GPU leaves SMs idle while the
-        other stream's call waits for them; two such calls each get half the SMs and run
-        side by side (two CP ranks sharing one GPU).  Larger calls keep every SM."""
-        if len(self.calls) < 2:
-            return 0
-        if all(self.call_cta_tiles(c) <= sms for c in self.calls):
-            return sms // 2
-        return 0
-
-    def call_algorithmic(self, c):
-        """(bytes, flops) one decode call must move / do."""
-        hl, hh, lo, hi, _, _ = c
-        Hs = hh - hl
-        toks = pages = 0
-        P = self.w.page_size
-        i = next(k for k, x in enumerate(self.calls) if x is c)
-        rng = self.ranges[i].cpu().tolist() if self.ranges is not None else None
-        for r, L in enumerate(self.w.ctx_lens):
-            if rng is not None:
-                lo, hi = rng[0][r], rng[1][r]
-            a, b = lo, (L if hi < 0 else min(hi, L))
-            if b > a:
-                toks += b - a
-                pages += (b - 1) // P - a // P + 1
-        rows = self.B * Hs
-        # with several KV heads a call reads the KV heads its query heads map to
-        Hkv = self.w.num_kv_heads
-        kv_read = 1 if Hkv == 1 else len({h // (self.H // Hkv) for h in range(hl, hh)})
-        return algorithmic(Hs, toks, rows, pages, kv_read)
-
-    def decode(self, c, q=None, bt=None, ctx=None, max_sms=0, ws=None):
-        inp = self.inp
-        ws = self.ws if ws is None else ws
-        hl, hh, lo, hi, out, lse = c
-        q = q if q is not None else inp.q
-        bt = bt if bt is not None else inp.block_table
-        ctx = ctx if ctx is not None else inp.ctx_lens
-        if self.ranges is not None or max_sms or inp.pool.dim() == 4:
-            i = next(k for k, x in enumerate(self.calls) if x is c)
-            rl = self.ranges[i, 0] if self.ranges is not None else None
-            rh = self.ranges[i, 1] if self.ranges is not None else None
-            self.S.splash_decode_attn_ex(q, inp.pool, bt, ctx, hl, hh, lo, hi, out, lse, ws,
-                                         self.w.scale, tok_lo_r=rl, tok_hi_r=rh,
-                                         max_sms=max_sms)
+    def decode(self, c, ws, max_sms=None):
+        inp, d = self.inp, self.dev
+        pool = inp.pool if c.pool == "pool1" else self.pool2
+        bt = d["bt1"] if c.pool == "pool1" else d["bt2"]
+        out, lse = self.outs[c.out]
+        sms = self.call_sms[id(c)] if max_sms is None else max_sms
+        rows = d[self.rows_key[id(c)]] if id(c) in self.rows_key else None
+        rl = rh = None
+        if c.share is not None:
+            rl, rh = d["ranges"][c.share, 0], d["ranges"][c.share, 1]
+        if rows is not None or rl is not None or sms or pool.dim() == 4:
+            self.S.splash_decode_attn_ex(inp.q, pool, bt, d["ctx"], c.head_lo, c.head_hi, c.tok_lo,
+                                         c.tok_hi, out, lse, ws, self.w.scale, tok_lo_r=rl,
+                                         tok_hi_r=rh, rows=rows, max_sms=sms)
         else:
-            self.S.splash_decode_attn(q, inp.pool, bt, ctx, hl, hh, lo, hi, out, lse, ws,
-                                      self.w.scale)
+            self.S.splash_decode_attn(inp.q, pool, bt, d["ctx"], c.head_lo, c.head_hi, c.tok_lo,
+                                      c.tok_hi, out, lse, ws, self.w.scale)
 
-    def run(self, q=None, bt=None, ctx=None, decode_events=None, row_events=None):
-        """One step.  decode_events: a (start, end) pair recorded around the step's
-        back-to-back decode calls; row_events: pairs around the merge and the migration."""
+    def run_phase(self, ph, max_sms=None):
         import torch
-        if decode_events is not None:
-            decode_events[0].record()
-        cur = torch.cuda.current_stream()
-        if len(self.calls) > 1:
-            fork = torch.cuda.Event()
-            fork.record(cur)
-            self.stream_b.wait_event(fork)
-        for k, c in enumerate(self.calls):
-            if k % 2:
-                with torch.cuda.stream(self.stream_b):
-                    self.decode(c, q, bt, ctx, max_sms=self.call_sms, ws=self.ws_b)
-            else:
-                self.decode(c, q, bt, ctx, max_sms=self.call_sms)
-        if len(self.calls) > 1:
-            join = torch.cuda.Event()
-            join.record(self.stream_b)
-            cur.wait_event(join)
-        if decode_events is not None:
-            decode_events[1].record()
-        # the handoff's migration does not depend on the merge: a small one runs on the
-        # second stream alongside the merge; a large one would contend with the merge and
-        # the decode tail for SMs and HBM (see the background-handoff measurement), so it
-        # runs after them
-        two = len(self.calls) > 1 and self.migrate_bytes() <= (64 << 20)
-        mig_stream = self.stream_b if two else cur
-        with torch.cuda.stream(mig_stream):
-            if row_events is not None:
-                row_events["kv_migrate"][0].record()
-            self.S.splash_kv_migrate(self.inp.pool, self.pool2, self.src_ids, self.dst_ids)
-            if row_events is not None:
-                row_events["kv_migrate"][1].record()
-        if self.merge:
-            if row_events is not None:
-                row_events["lse_merge"][0].record()
-            self.S.splash_lse_merge(self.po, self.pl, self.out, self.lse)
-            if row_events is not None:
-                row_events["lse_merge"][1].record()
-        if two:
-            done = torch.cuda.Event()
-            done.record(self.stream_b)
-            cur.wait_event(done)
+        if ph[0] == "decode":
+            calls = ph[1]
+            cur = torch.cuda.current_stream()
+            if len(calls) > 1:
+                fork = torch.cuda.Event()
+                fork.record(cur)
+                self.stream_b.wait_event(fork)
+            for k, c in enumerate(calls):
+                if k % 2:
+                    with torch.cuda.stream(self.stream_b):
+                        self.decode(c, self.ws_b, max_sms)
+                else:
+                    self.decode(c, self.ws, max_sms)
+            if len(calls) > 1:
+                join = torch.cuda.Event()
+                join.record(self.stream_b)
+                cur.wait_event(join)
+        elif ph[0] == "merge":
+            self.S.splash_lse_merge(self.po[:ph[1]], self.pl[:ph[1]], self.out, self.lse)
+        else:
+            self.migrate()
+
+    def migrate(self):
+        self.S.splash_kv_migrate(self.inp.pool, self.pool2, self.src_ids, self.dst_ids)
+
+    def run(self, events=None):
+        """One step; events: one (start, end) pair per phase, recorded around it."""
+        for i, ph in enumerate(self.phases):
+            if events is not None:
+                events[i][0].record()
+            self.run_phase(ph)
+            if events is not None:
+                events[i][1].record()
 
     def run_background_handoff(self, side2, max_sms, dec_events, join_event):
-        """The step's decode calls on the current stream with at most max_sms SMs, while
-        the handoff's page migration runs on stream side2 (forked from the current
-        stream; joined back at the end).  dec_events brackets the decode calls."""
+        """The step's first decode phase on the current stream with at most max_sms SMs,
+        while the handoff's page migration runs on stream side2 (forked from the current
+        stream; joined back at the end).  dec_events brackets the decode phase."""
         import torch
         cur = torch.cuda.current_stream()
         fork = torch.cuda.Event()
         fork.record(cur)
         side2.wait_event(fork)
         with torch.cuda.stream(side2):
-            self.S.splash_kv_migrate(self.inp.pool, self.pool2, self.src_ids, self.dst_ids)
+            self.migrate()
             join_event.record(side2)
         dec_events[0].record()
-        for c in self.calls:
-            self.decode(c, max_sms=max_sms)
+        self.run_phase(self.phases[0], max_sms=max_sms)
         dec_events[1].record()
         cur.wait_event(join_event)
 
-    def merge_bytes(self):
+    def merge_bytes(self, n):
         """Bytes splash_lse_merge must move: every share's fp32 rows read once, one written."""
-        n = self.po.shape[0] if self.merge else 0
         return (n + 1) * self.B * self.H * (512 * 4 + 4)
 
     def migrate_bytes(self):
-        return 2 * self.page_bytes * int(self.src_ids.numel())
+        return 2 * self.page_bytes * int(self.src_ids.numel()) if self.mig is not None else 0
 
 
 def pack(tensors, device):
@@ -458,16 +584,6 @@ def pack(tensors, device):
     return buf, views
 
 
-def algorithmic(Hs, tokens_in_call, rows, pages, kv_heads_read=1):
-    """Bytes and flops one decode call must move / do: every KV token once (576 bf16
-    per KV head the call reads), q rows (576 bf16), fp32 out rows + lse, 4 bytes per
-    page id."""
-    bytes_ = (tokens_in_call * 576 * 2 * kv_heads_read + rows * 576 * 2 + rows * (512 * 4 + 4)
-              + pages * 4)
-    flops = 2.0 * tokens_in_call * Hs * (576 + 512)
-    return bytes_, flops
-
-
 # ----------------------------------------------------------------------------- arms
 
 def run_ours(args, world, rank, local):
@@ -482,24 +598,16 @@ def run_ours(args, world, rank, local):
     # weak scaling: every rank owns its own batch of the workload (own seed)
     inp = W.make_decode_inputs(w.ctx_lens, w.num_heads, w.page_size, w.seed + 1000 * rank,
                                device=device, spare_frac=w.spare_frac, num_kv_heads=w.num_kv_heads)
-    # q, block table and context lengths share one buffer: the end-to-end leg copies
-    # them in with one transfer
-    ins = [inp.q, inp.block_table, inp.ctx_lens]
-    if w.per_request_splits:
-        ins.append(W.per_request_ranges(w))
-    in_pack, views = pack(ins, device)
-    inp.q, inp.block_table, inp.ctx_lens = views[:3]
-    step = Step(w, inp, device, ranges=views[3] if w.per_request_splits else None,
-                call_sms=args.call_sms)
+    step = Step(w, inp, device, call_sms=args.call_sms)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     K, Wm = args.steps, args.warmup
+    nph = len(step.phases)
 
     # one eager pass (caches the per-device state), then two sets of CUDA graphs of one
     # step each: plain graphs for the headline timing, and instrumented graphs with
-    # in-graph events around the decode calls, the merge and the migration for the
-    # per-row breakdown.  Event nodes inside a graph end the programmatic-dependent-
-    # launch overlap between neighbouring kernels and add latency, so they stay out of
-    # the headline graphs.
+    # in-graph events around every phase for the per-row breakdown.  Event nodes inside
+    # a graph end the programmatic-dependent-launch overlap between neighbouring kernels
+    # and add latency, so they stay out of the headline graphs.
     step.run()
     torch.cuda.synchronize()
 
@@ -518,15 +626,13 @@ def run_ours(args, world, rank, local):
         return g
 
     graphs = [capture() for _ in range(max(K, 1))]
-    inst, dec_ev, row_ev = [], [], []
+    inst, ph_ev = [], []
     for k in range(max(K, 1)):
-        evs = (new_event(), new_event())
-        rows = {n: (new_event(), new_event()) for n in ("lse_merge", "kv_migrate")}
-        if None in evs or any(e is None for pair in rows.values() for e in pair):
+        evs = [(new_event(), new_event()) for _ in range(nph)]
+        if any(e is None for pair in evs for e in pair):
             break
-        inst.append(capture(decode_events=evs, row_events=rows))
-        dec_ev.append(evs)
-        row_ev.append(rows)
+        inst.append(capture(events=evs))
+        ph_ev.append(evs)
     stream = torch.cuda.current_stream(device)
     for k in range(Wm):
         flush.zero_()
@@ -547,24 +653,24 @@ def run_ours(args, world, rank, local):
     barrier(world)
     step_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
 
-    # breakdown: K instrumented steps, same flush
-    ncalls = len(step.calls)
+    # breakdown: K instrumented steps, same flush; mean time of every phase
+    ph_us = None
     if len(inst) == max(K, 1):
         for k in range(K):
             flush.zero_()
             inst[k].replay()
         torch.cuda.synchronize()
-        dec_ms = [dec_ev[k][0].elapsed_time(dec_ev[k][1]) / ncalls for k in range(K)]
-        dec_src = (f"CUDA events captured inside instrumented step graphs around the step's "
-                   f"{ncalls} back-to-back decode call(s) (a second timed pass of K steps); "
-                   f"per call = their span / {ncalls}")
-    else:   # events cannot be captured: time graph replays of single decode calls
-        row_ev = [None]
-        dec_ms = []
-        for c in step.calls[:2]:
+        ph_us = [statistics.mean(ph_ev[k][i][0].elapsed_time(ph_ev[k][i][1]) for k in range(K)) * 1e3
+                 for i in range(nph)]
+        dec_src = ("CUDA events captured inside instrumented step graphs around every decode "
+                   "phase (a second timed pass of K steps)")
+    else:   # events cannot be captured: time graph replays of each decode phase alone
+        ph_us = []
+        for ph in step.phases:
             g1 = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g1, stream=side):
-                step.decode(c)
+                step.run_phase(ph)
+            t = []
             for k in range(K):
                 flush.zero_()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -572,12 +678,14 @@ def run_ours(args, world, rank, local):
                 g1.replay()
                 b.record(stream)
                 torch.cuda.synchronize()
-                dec_ms.append(a.elapsed_time(b))
-        dec_src = "CUDA events around graph replays of one decode call"
-    # background handoff: the decode calls on all but RESERVED SMs while the page
-    # migration runs on a second stream, against the decode calls alone on every SM
+                t.append(a.elapsed_time(b) * 1e3)
+            ph_us.append(statistics.mean(t))
+        dec_src = "CUDA events around graph replays of each decode phase alone"
+
+    # background handoff: the first decode phase on all but RESERVED SMs while the page
+    # migration runs on a second stream, against that phase alone on every SM
     handoff = None
-    if len(inst) == max(K, 1):
+    if step.mig is not None and len(inst) == max(K, 1):
         reserved = args.reserved_sms
         side2 = torch.cuda.Stream(device)
         g_alone, g_bg, ev_alone, ev_bg, ev_span = [], [], [], [], []
@@ -586,8 +694,7 @@ def run_ours(args, world, rank, local):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=side):
                 ea[0].record()
-                for c in step.calls:
-                    step.decode(c)
+                step.run_phase(step.phases[0])
                 ea[1].record()
             g_alone.append(g)
             ev_alone.append(ea)
@@ -595,9 +702,7 @@ def run_ours(args, world, rank, local):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=side):
                 es[0].record()
-                step.run_background_handoff(side2, torch.cuda.get_device_properties(device)
-                                            .multi_processor_count - reserved, eb,
-                                            torch.cuda.Event())
+                step.run_background_handoff(side2, step.sms - reserved, eb, torch.cuda.Event())
                 es[1].record()
             g_bg.append(g)
             ev_bg.append(eb)
@@ -610,27 +715,16 @@ def run_ours(args, world, rank, local):
         t_alone = statistics.mean(a.elapsed_time(b) for a, b in ev_alone) * 1e3
         t_dec_bg = statistics.mean(a.elapsed_time(b) for a, b in ev_bg) * 1e3
         t_span = statistics.mean(a.elapsed_time(b) for a, b in ev_span) * 1e3
-        t_mig = statistics.mean(row_ev[k]["kv_migrate"][0].elapsed_time(row_ev[k]["kv_migrate"][1])
-                                for k in range(K)) * 1e3
+        t_mig = ph_us[[i for i, ph in enumerate(step.phases) if ph[0] == "migrate"][0]]
         handoff = {
             "reserved_sms": reserved, "migrate_bytes": step.migrate_bytes(),
             "decode_us_alone": t_alone, "decode_us_with_background_migrate": t_dec_bg,
             "decode_slowdown_pct": 100.0 * (t_dec_bg - t_alone) / t_alone,
             "overlapped_us": t_span, "serial_us": t_alone + t_mig,
-            "note": "decode calls with max_sms = SMs - reserved on one stream, splash_kv_migrate "
-                    "on a second stream of the same graph; serial = decode alone + migrate alone",
+            "note": "first decode phase with max_sms = SMs - reserved on one stream, "
+                    "splash_kv_migrate on a second stream of the same graph; serial = decode "
+                    "alone + migrate alone",
         }
-    rows_report = {}
-    if row_ev[0] is not None:
-        mig_us = statistics.mean(row_ev[k]["kv_migrate"][0].elapsed_time(row_ev[k]["kv_migrate"][1])
-                                 for k in range(K)) * 1e3
-        rows_report["kv_migrate"] = {"us": mig_us, "bytes": step.migrate_bytes(),
-                                     "gb_s": step.migrate_bytes() / mig_us / 1e3}
-        if step.merge:
-            mer_us = statistics.mean(row_ev[k]["lse_merge"][0].elapsed_time(row_ev[k]["lse_merge"][1])
-                                     for k in range(K)) * 1e3
-            rows_report["lse_merge"] = {"us": mer_us, "bytes": step.merge_bytes(),
-                                        "gb_s": step.merge_bytes() / mer_us / 1e3}
     total_ms = max_over_ranks(sum(step_ms), world, device)
     status = S.splash_workspace_status(step.ws)
     if step.ws_b is not None:
@@ -638,10 +732,10 @@ def run_ours(args, world, rank, local):
     if status != 0:
         raise RuntimeError(f"device status word set: {status}")
 
-    # end to end through the public API with host buffers: the pinned q / block table /
-    # context lengths copied in (one transfer of the packed inputs), the step, and the
-    # merged out / lse copied back (one transfer), every step
-    in_h = in_pack.cpu().pin_memory()
+    # end to end through the public API with host buffers: the pinned inputs (q, block
+    # tables, context lengths, request rows, ranges) copied in with one transfer, the
+    # step, and its out / lse copied back with one transfer, every step
+    in_h = step.in_pack.cpu().pin_memory()
     out_h = torch.empty(step.out_pack.shape, dtype=torch.uint8).pin_memory()
     h2d = in_h.numel()
     d2h = out_h.numel()
@@ -650,7 +744,7 @@ def run_ours(args, world, rank, local):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        in_pack.copy_(in_h, non_blocking=True)      # the graphs read the views of in_pack
+        step.in_pack.copy_(in_h, non_blocking=True)   # the graphs read views of in_pack
         graphs[k % len(graphs)].replay()
         out_h.copy_(step.out_pack, non_blocking=True)
         stream.synchronize()
@@ -658,38 +752,61 @@ def run_ours(args, world, rank, local):
             e2e_ms.append((time.perf_counter() - t0) * 1e3)
     e2e_total = max_over_ranks(sum(e2e_ms), world, device)
 
-    tokens = w.kv_tokens
+    tokens = decoded_tokens(w, step.phases, step.ranges_host)
     total_tokens = sum_over_ranks(float(tokens), world, device)
     value = total_tokens * K / (total_ms / 1e3)
     e2e_value = total_tokens * K / (e2e_total / 1e3)
 
-    # roofline of the dominant kernel: the decode call (plan + tcgen05 decode + combine)
+    # roofline of the dominant kernel, the decode call (plan + tcgen05 decode + combine):
+    # the algorithmic bytes of every decode call of the step / the decode phases' time
     hbm_peak, bf16_peak, peak_src = measured_peaks()
-    call_bytes = [step.call_algorithmic(c) for c in step.calls]
-    alg_bytes = sum(b for b, _ in call_bytes) / len(call_bytes)
-    alg_flops = sum(f for _, f in call_bytes) / len(call_bytes)
-    dec_avg_s = statistics.mean(dec_ms) / 1e3
-    achieved_gbs = alg_bytes / dec_avg_s / 1e9
-    achieved_tfs = alg_flops / dec_avg_s / 1e12
+    dec_idx = [i for i, ph in enumerate(step.phases) if ph[0] == "decode"]
+    calls = step.decode_calls()
+    alg = [call_algorithmic(w, c, step.ranges_host) for c in calls]
+    alg_bytes = sum(b for b, _ in alg)
+    alg_flops = sum(f for _, f in alg)
+    dec_s = sum(ph_us[i] for i in dec_idx) / 1e6
+    achieved_gbs = alg_bytes / dec_s / 1e9
+    achieved_tfs = alg_flops / dec_s / 1e12
     traffic = ncu_traffic(args.workload)
     clocks = clk.summary()
+    rows_report = {}
+    for i, ph in enumerate(step.phases):
+        if ph[0] == "migrate":
+            b = step.migrate_bytes()
+            rows_report["kv_migrate"] = {"us": ph_us[i], "bytes": b, "gb_s": b / ph_us[i] / 1e3,
+                                         "frac_of_hbm": b / ph_us[i] / 1e3 / hbm_peak}
+        elif ph[0] == "merge":
+            b = step.merge_bytes(ph[1])
+            rows_report["lse_merge"] = {"us": ph_us[i], "bytes": b, "gb_s": b / ph_us[i] / 1e3,
+                                        "frac_of_hbm": b / ph_us[i] / 1e3 / hbm_peak}
+    phases_report = []
+    for i, ph in enumerate(step.phases):
+        e = {"phase": ph[0], "us": ph_us[i]}
+        if ph[0] == "decode":
+            pa = [call_algorithmic(w, c, step.ranges_host) for c in ph[1]]
+            e["calls"] = len(ph[1])
+            e["alg_bytes"] = sum(b for b, _ in pa)
+            e["frac_of_hbm"] = e["alg_bytes"] / ph_us[i] / 1e3 / hbm_peak
+        phases_report.append(e)
 
     line = None
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(w, inp, args.cpu_seconds)
+        launch = ("calls of a decode phase alternate between two streams, one workspace each"
+                  if any(ph[0] == "decode" and len(ph[1]) > 1 for ph in step.phases) else
+                  "one stream")
+        small = sorted({s for s in step.call_sms.values() if s})
+        if small:
+            launch += f"; calls that fit in one wave limited to {small[0]} of {step.sms} SMs each"
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": Wm, "ms_per_step": total_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {
-                "workload": w.name, "global_batch": w.batch * world, "seq_len": max(w.ctx_lens),
-                "heads": w.num_heads, "page_size": w.page_size, "kv_tokens_per_rank": tokens,
-                "parallelism": f"replicas{world}" if world > 1 else "single",
-                "step": step.pattern + "; captured as one CUDA graph",
-                "l2": "512 MB flush write before every timed step",
-            },
+            "config": workload_config(w, step.phases, world),
+            "launch": launch + "; each step captured as one CUDA graph",
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_total / K},
@@ -697,11 +814,13 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak,
                          "unit": "GB/s", "frac": achieved_gbs / hbm_peak, "traffic": traffic,
                          "kernel": "splash_decode_attn call (plan + tcgen05 decode + combine)",
-                         "alg_bytes_per_launch": alg_bytes, "launch_us": dec_avg_s * 1e6,
+                         "alg_bytes_per_step": alg_bytes, "decode_us_per_step": dec_s * 1e6,
+                         "decode_calls_per_step": len(calls),
                          "timing": dec_src, "peak_source": f"{peak_src} hbm_gbs",
                          "tflops": achieved_tfs,
                          "tensor_frac_of_bf16_peak": achieved_tfs / bf16_peak},
-            "other_rows": {k: dict(v, frac_of_hbm=v["gb_s"] / hbm_peak) for k, v in rows_report.items()},
+            "phases": phases_report,
+            "other_rows": rows_report,
             "background_handoff": handoff,
             "cpu_baseline": cpu,
         }
@@ -712,7 +831,6 @@ def run_ours(args, world, rank, local):
 def cpu_baseline(w, inp, seconds: float):
     """The fp64 oracle, as it stands, on this host's cores over a bounded sample of the
     same workload (whole requests, all heads), in KV-tokens/s."""
-    import numpy as np
     import oracle
     q = oracle.bf16_bits(inp.q)
     pool = oracle.bf16_bits(inp.pool)
@@ -734,47 +852,125 @@ def cpu_baseline(w, inp, seconds: float):
                       f"{toks} KV tokens, {t_total:.1f} s"}
 
 
+def reference_step(w, phases, q, pool, bt, ctx, sample, mig, pool2, bt2, ranges):
+    """One step of the workload's pattern run by the fp64 oracle over the requests in
+    `sample` (all heads): the same phases as the GPU step, restricted to the sample."""
+    import numpy as np
+    import oracle
+    B, H = len(ctx), w.num_heads
+    out = np.full((B, H, 512), np.nan)
+    lse = np.full((B, H), np.nan)
+    parts = {}
+    sample = np.asarray(sample)
+    for ph in phases:
+        if ph[0] == "decode":
+            for c in ph[1]:
+                rows = sample if c.rows is None else np.intersect1d(sample, np.asarray(c.rows))
+                if rows.size == 0:
+                    continue
+                p, t = (pool, bt) if c.pool == "pool1" else (pool2, bt2)
+                if c.share is not None:
+                    lo = np.asarray(ranges[c.share][0])[rows]
+                    hi = np.asarray(ranges[c.share][1])[rows]
+                    res = [oracle.decode_attn(q[r:r + 1], p, t[r:r + 1], ctx[r:r + 1], w.scale,
+                                              c.head_lo, c.head_hi, int(a), int(b))
+                           for r, a, b in zip(rows, lo, hi)]
+                    o = np.concatenate([x[0] for x in res])
+                    l = np.concatenate([x[1] for x in res])
+                else:
+                    o, l = oracle.decode_attn(q[rows], p, t[rows], ctx[rows], w.scale, c.head_lo,
+                                              c.head_hi, c.tok_lo, c.tok_hi)
+                if c.out.startswith("part"):
+                    parts[c.out] = (rows, o, l)
+                else:
+                    out[rows, c.head_lo:c.head_hi] = o[:, c.head_lo:c.head_hi]
+                    lse[rows, c.head_lo:c.head_hi] = l[:, c.head_lo:c.head_hi]
+        elif ph[0] == "merge":
+            rows = parts["part0"][0]
+            po = np.stack([parts[f"part{i}"][1] for i in range(ph[1])])
+            pl = np.stack([parts[f"part{i}"][2] for i in range(ph[1])])
+            out[rows], lse[rows] = oracle.lse_merge(po, pl)
+        else:
+            moved = [r for r in mig.requests if r in set(sample.tolist())]
+            if moved:
+                src = np.concatenate([bt[r, :(ctx[r] + w.page_size - 1) // w.page_size]
+                                      for r in moved]).astype(np.int32)
+                dst = np.concatenate([bt2[r, :(ctx[r] + w.page_size - 1) // w.page_size]
+                                      for r in moved]).astype(np.int32)
+                oracle.kv_migrate(pool, pool2, src, dst)
+    return out, lse
+
+
 def run_reference(args, world, rank, local):
-    """The fp64 C oracle as the reference arm, timed on the host cores."""
+    """The fp64 C oracle as the reference arm, timed on the host cores: every step runs
+    the workload's own step pattern (step_pattern) over a bounded sample of its
+    requests."""
     if rank != 0:
         return None
+    import numpy as np
     import torch
     import oracle
     from layout_agnostic_paged_gb300 import workloads as W
     w = W.ALL[args.workload]()
-    inp = W.make_decode_inputs(w.ctx_lens, w.num_heads, w.page_size, w.seed, device="cpu"
-                               if w.kv_tokens <= 2_000_000 else "cuda:0", spare_frac=w.spare_frac,
-                               num_kv_heads=w.num_kv_heads)
+    dev = "cuda:0" if (w.kv_tokens > 2_000_000 and torch.cuda.is_available()) else "cpu"
+    inp = W.make_decode_inputs(w.ctx_lens, w.num_heads, w.page_size, w.seed, device=dev,
+                               spare_frac=w.spare_frac, num_kv_heads=w.num_kv_heads)
+    mig = W.make_migration(inp, w.migrate_frac, seed=w.seed) if w.migrate_frac > 0 else None
+    phases = step_pattern(w, mig.requests if mig else None)
     q = oracle.bf16_bits(inp.q)
     pool = oracle.bf16_bits(inp.pool)
     bt = inp.block_table.cpu().numpy()
     ctx = inp.ctx_lens.cpu().numpy()
-    # each step: a bounded sample of whole requests (all heads) sized so that
-    # warm-up + steps stay within a few minutes
+    pool2 = bt2 = None
+    if mig is not None:
+        pool2 = np.zeros((mig.dst_num_pages,) + pool.shape[1:], dtype=np.uint16)
+        bt2 = np.full(bt.shape, -1, dtype=np.int32)
+        bt2[mig.requests] = mig.new_block_table.numpy()
+    del inp
+    ranges = per_request_ranges_or_none(w)
+    # size the sample (whole requests, in a seeded order, every kind of call covered) so
+    # that warm-up + steps stay within about two minutes
+    order = np.random.default_rng(w.seed + 29).permutation(len(ctx))
+    if mig is not None:   # alternate moved and remaining requests so both reruns run
+        mv = [r for r in order if r in set(mig.requests)]
+        kp = [r for r in order if r not in set(mig.requests)]
+        order = np.array([x for pair in zip(kp, mv) for x in pair] + kp[len(mv):] + mv[len(kp):])
     t0 = time.perf_counter()
-    oracle.decode_attn(q[:1], pool, bt[:1], ctx[:1], w.scale)
-    per_req = max(time.perf_counter() - t0, 1e-3)
+    reference_step(w, phases, q, pool, bt, ctx, order[:2], mig, pool2, bt2, ranges)
+    per_tok = max(time.perf_counter() - t0, 1e-3) / max(1, int(ctx[order[:2]].sum()))
     budget = 120.0 / max(1, args.steps + args.warmup)
-    n_req = max(1, min(len(ctx), int(budget / per_req)))
-    times, toks = [], int(ctx[:n_req].sum())
+    n_req, acc = 0, 0
+    while n_req < len(order) and (acc + ctx[order[n_req]]) * per_tok <= budget:
+        acc += int(ctx[order[n_req]])
+        n_req += 1
+    n_req = max(n_req, min(2, len(order)))
+    sample = np.sort(order[:n_req])
+    sw = W.Workload(w.name, tuple(int(ctx[r]) for r in sample), w.num_heads, w.page_size, w.seed)
+    sub_phases = [(ph[0], [CallSpec(c.head_lo, c.head_hi, c.tok_lo, c.tok_hi,
+                                    None if c.rows is None else tuple(
+                                        i for i, r in enumerate(sample) if r in set(c.rows)),
+                                    c.pool, c.share, c.out) for c in ph[1]])
+                  if ph[0] == "decode" else ph for ph in phases]
+    toks = decoded_tokens(sw, sub_phases, None if ranges is None else
+                          [[[row[r] for r in sample] for row in share] for share in ranges])
+    times = []
     for k in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.decode_attn(q[:n_req], pool, bt[:n_req], ctx[:n_req], w.scale)
+        reference_step(w, phases, q, pool, bt, ctx, sample, mig, pool2, bt2, ranges)
         dt = time.perf_counter() - t0
         if k >= args.warmup:
             times.append(dt)
     total = sum(times)
     value = toks * args.steps / total
-    sample = f"{n_req} of {len(ctx)} requests (all {w.num_heads} heads) per step, {toks} KV tokens"
+    desc = (f"{n_req} of {len(ctx)} requests (all {w.num_heads} heads) per step through the "
+            f"step's phases, {toks} decoded KV tokens")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "global_batch": w.batch,
-                                        "seq_len": max(w.ctx_lens), "heads": w.num_heads,
-                                        "page_size": w.page_size},
+        "data": "synthetic", "config": workload_config(w, phases, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

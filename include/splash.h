@@ -160,7 +160,7 @@ SPLASH_API int splash_decode_attn(const splash_attn_desc* desc, const void* q, c
  *                   pool is bf16 [num_pages][Hkv][P][576] and query head h reads KV head
  *                   h / (H / Hkv).  H must be a multiple of Hkv.  H / Hkv must be at most 64
  *                   or a multiple of 64, and head_lo a multiple of min(H / Hkv, 64); other
- *                   shapes return SPLASH_ERR_UNSUPPORTED, as does the CUDA-core kernel.
+ *                   shapes return SPLASH_ERR_UNSUPPORTED.
  */
 typedef struct {
     const int32_t* tok_lo;
@@ -208,14 +208,25 @@ SPLASH_API int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_
  *     contents (each call rewrites all of it that it reads).  Calls that may
  *     overlap on the GPU (different streams, or graphs replayed concurrently)
  *     race on it: serialise them.
- *   - The device status word of splash_workspace_status is not reachable for
- *     this entry point.
+ *   - The device status word (SPLASH_DEVICE_* bits) of the last call on the
+ *     device is read with splash_noalloc_status.
  */
 SPLASH_API int splash_decode_attn_noalloc(const splash_attn_desc* desc, const void* q,
                                           const void* kv_pool, const int32_t* block_table,
                                           const int32_t* ctx_lens, int head_lo, int head_hi,
                                           int64_t tok_lo, int64_t tok_hi, float* out, float* lse,
                                           splash_stream_t stream);
+
+/*
+ * Device status word of the most recent splash_decode_attn_noalloc call on the
+ * current device (the SPLASH_DEVICE_* bits that splash_workspace_status reports
+ * for a caller workspace).  Like splash_decode_attn_noalloc it has no counterpart
+ * in the paper.  Synchronises `stream` (the stream of that call), then copies 4
+ * bytes from the library's scratch to *flags (host pointer).  The word belongs to
+ * the last call on the device, whichever stream issued it.  Allocates nothing.
+ * Returns SPLASH_OK or an error.
+ */
+SPLASH_API int splash_noalloc_status(uint32_t* flags, splash_stream_t stream);
 
 /*
  * Log-sum-exp merge of S partial results over disjoint token sets (the CP

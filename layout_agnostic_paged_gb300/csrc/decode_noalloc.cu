@@ -60,4 +60,20 @@ int splash_decode_attn_noalloc(const splash_attn_desc* desc, const void* q, cons
                               tok_hi, out, lse, scratch, splash::kNoAllocScratchBytes, stream);
 }
 
+// The status word lives at the start of the scratch array (the plan header), where the
+// decode kernels of the last splash_decode_attn_noalloc call on this device left it.
+int splash_noalloc_status(uint32_t* flags, splash_stream_t stream) {
+    if (!flags) return SPLASH_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SPLASH_ERR_CUDA;
+    void* scratch = nullptr;
+    const int st = splash::scratch_address(dev, &scratch);
+    if (st != SPLASH_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SPLASH_ERR_CUDA;
+    if (cudaMemcpy(flags, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SPLASH_ERR_CUDA;
+    return SPLASH_OK;
+}
+
 }  // extern "C"

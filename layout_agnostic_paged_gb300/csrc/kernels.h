@@ -68,8 +68,4 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& map_q,
                              const CUtensorMap& map_kv, int head_groups, int group_heads,
                              cudaStream_t stream);
 
-// SIMT decode kernel: heads in groups of kSimtHeads, one CTA per (CTA group, head group).
-constexpr int kSimtHeads = 16;
-cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
-
 }  // namespace splash

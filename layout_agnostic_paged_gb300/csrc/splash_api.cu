@@ -48,17 +48,6 @@ int validate_desc(const splash_attn_desc* d) {
     return SPLASH_OK;
 }
 
-// Which decode kernel runs: the tensor-core kernel; the CUDA-core kernel only when
-// SPLASH_DECODE_KERNEL=simt is set in the environment (a GPU cross-check).
-bool use_simt() {
-    static int v = -1;
-    if (v < 0) {
-        const char* e = getenv("SPLASH_DECODE_KERNEL");
-        v = (e && strcmp(e, "simt") == 0) ? 1 : 0;
-    }
-    return v == 1;
-}
-
 // Launch geometry of the decode kernel for a head slice of Hs heads.
 struct Geometry {
     int head_groups;  // CTAs per CTA group (one per head group)
@@ -70,11 +59,7 @@ struct Geometry {
 // stay within one KV head's query heads).
 Geometry decode_geometry(int Hs, int sms, int kv_group_heads = 0) {
     Geometry g;
-    if (use_simt()) {
-        g.head_groups = (Hs + kSimtHeads - 1) / kSimtHeads;
-        g.group_heads = kSimtHeads;
-        g.num_groups = (2 * sms) / g.head_groups;
-    } else if (kv_group_heads > 0) {
+    if (kv_group_heads > 0) {
         g.group_heads = kv_group_heads;
         g.head_groups = (Hs + kv_group_heads - 1) / kv_group_heads;
         g.num_groups = sms / g.head_groups;
@@ -200,7 +185,7 @@ int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext*
         const int per_kv = desc->num_heads / kv_heads;
         if (per_kv > kTcMaxGroupHeads && per_kv % kTcMaxGroupHeads != 0) return SPLASH_ERR_UNSUPPORTED;
         kv_group_heads = per_kv < kTcMaxGroupHeads ? per_kv : kTcMaxGroupHeads;
-        if (head_lo % kv_group_heads != 0 || use_simt()) return SPLASH_ERR_UNSUPPORTED;
+        if (head_lo % kv_group_heads != 0) return SPLASH_ERR_UNSUPPORTED;
         if (int64_t(desc->num_pages) * kv_heads * desc->page_size >= (int64_t(1) << 31))
             return SPLASH_ERR_UNSUPPORTED;
     }
@@ -246,9 +231,7 @@ int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext*
     a.kv_heads = kv_heads;
     a.q_per_kv = desc->num_heads / kv_heads;
     a.scale = desc->scale;
-    if (use_simt()) {
-        if (launch_decode_simt(a, stream) != cudaSuccess) return SPLASH_ERR_CUDA;
-    } else {
+    {
         CUtensorMap mq, mkv;
         const uint32_t qbox = uint32_t(tc_pad_heads(g.group_heads));
         if (!encode_rows_576(&mq, q, uint64_t(num_rows) * desc->num_heads, qbox)) return SPLASH_ERR_CUDA;

@@ -25,7 +25,7 @@ SPLASH_DEVICE_TIMEOUT = 1
 SPLASH_DEVICE_BAD_INPUT = 2
 
 EXPORTED = ("splash_decode_workspace_size", "splash_decode_attn", "splash_decode_attn_ex",
-            "splash_decode_attn_noalloc",
+            "splash_decode_attn_noalloc", "splash_noalloc_status",
             "splash_lse_merge", "splash_kv_migrate", "splash_workspace_status",
             "splash_status_string")
 
@@ -74,6 +74,8 @@ def load_library(path: str | None = None):
         lib.splash_decode_attn_ex.restype = i32
         lib.splash_decode_attn_noalloc.argtypes = [dp, vp, vp, vp, vp, i32, i32, i64, i64, vp, vp, vp]
         lib.splash_decode_attn_noalloc.restype = i32
+        lib.splash_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+        lib.splash_noalloc_status.restype = i32
         lib.splash_lse_merge.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
         lib.splash_lse_merge.restype = i32
         lib.splash_kv_migrate.argtypes = [vp, vp, sz, vp, vp, i32, ctypes.c_int32, ctypes.c_int32, vp]
@@ -228,6 +230,18 @@ def splash_decode_attn_noalloc(q: torch.Tensor, kv_pool: torch.Tensor, block_tab
             _stream(stream))
     if rc != SPLASH_OK:
         raise SplashError(rc, "splash_decode_attn_noalloc")
+
+
+def splash_noalloc_status(device=None, stream=None) -> int:
+    """Synchronises the stream and returns the SPLASH_DEVICE_* bits of the last
+    splash_decode_attn_noalloc call on the device."""
+    flags = ctypes.c_uint32(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        rc = load_library().splash_noalloc_status(ctypes.byref(flags), _stream(stream))
+    if rc != SPLASH_OK:
+        raise SplashError(rc, "splash_noalloc_status")
+    return int(flags.value)
 
 
 def splash_lse_merge(part_out: torch.Tensor, part_lse: torch.Tensor, out: torch.Tensor,

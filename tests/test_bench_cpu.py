@@ -31,54 +31,104 @@ def test_bench_module_imports_without_gpu():
     assert len(bench.kernel_source_hash()) == 16
 
 
-def _fake_step(w, calls, ranges=None):
-    """A bench Step holding only what the call-size logic reads (no device buffers)."""
+def _bench():
     sys.path.insert(0, ROOT)
     import bench
-    st = bench.Step.__new__(bench.Step)
-    st.w, st.calls, st.ranges = w, calls, ranges
-    return st
+    return bench
 
 
-def test_small_two_call_steps_get_half_the_sms():
-    """A multi-call step whose calls each fit in one wave (128-token tiles x 64-head
-    groups <= SMs) gives every call half the SMs; larger calls and single calls keep
-    every SM."""
-    sys.path.insert(0, ROOT)
-    import bench
+def test_step_patterns_follow_each_configuration():
+    """Each workload's step is the calls its configuration defines: ragged + handoff =
+    whole-batch decode, migration, decode rerun as two request-subset calls on the two
+    pools; CP = token-share calls then the merge; head shards = one call per shard;
+    full heads and tiny = one call."""
+    bench = _bench()
     from layout_agnostic_paged_gb300 import workloads as W
-    Step = bench.Step
+    w = W.ragged_handoff()
+    moved = [3, 7, 100]
+    ph = bench.step_pattern(w, moved)
+    assert [p[0] for p in ph] == ["decode", "migrate", "decode"]
+    (pre,), post = ph[0][1], ph[2][1]
+    assert pre.rows is None and pre.out == "pre" and (pre.head_lo, pre.head_hi) == (0, 128)
+    assert [c.pool for c in post] == ["pool1", "pool2"]
+    assert post[1].rows == (3, 7, 100) and len(post[0].rows) == w.batch - 3
+    assert set(post[0].rows) | set(post[1].rows) == set(range(w.batch))
+    # the step decodes the batch twice, for every head
+    assert bench.decoded_tokens(w, ph) == 2 * w.kv_tokens
+    cp = bench.step_pattern(W.cp_long())
+    assert [p[0] for p in cp] == ["decode", "merge"] and cp[1][1] == 8
+    assert [(c.tok_lo, c.tok_hi) for c in cp[0][1]][:2] == [(0, 8192), (8192, 16384)]
+    assert cp[0][1][-1].tok_hi == -1
+    assert bench.decoded_tokens(W.cp_long(), cp) == W.cp_long().kv_tokens
+    hs = bench.step_pattern(W.head_shard())
+    assert [(c.head_lo, c.head_hi) for c in hs[0][1]] == [(16 * i, 16 * i + 16) for i in range(8)]
+    assert bench.decoded_tokens(W.head_shard(), hs) == W.head_shard().kv_tokens
+    for name in ("full_heads", "tiny"):
+        p = bench.step_pattern(W.ALL[name]())
+        assert len(p) == 1 and len(p[0][1]) == 1 and p[0][1][0].rows is None
+
+
+def test_small_two_call_phases_get_half_the_sms():
+    """A phase of several calls whose calls each fit in one wave (128-token tiles x
+    64-head groups <= SMs) gives every call half the SMs; larger calls and single calls
+    keep every SM."""
+    bench = _bench()
+    from layout_agnostic_paged_gb300 import workloads as W
+    C = bench.CallSpec
     fh = W.full_heads()                       # 16 x 1024 tokens, 128 heads
-    shares = [(0, 128, 0, 512, "out0", None), (0, 128, 512, -1, "out1", None)]
-    st = _fake_step(fh, shares)
-    assert [Step.call_cta_tiles(st, c) for c in shares] == [16 * 4 * 2, 16 * 4 * 2]
-    assert Step.pick_call_sms(st, 152) == 76
-    assert Step.pick_call_sms(st, 100) == 0   # 128 CTA-tiles no longer fit in one wave
-    one = _fake_step(fh, shares[:1])
-    assert Step.pick_call_sms(one, 152) == 0
+    shares = [C(0, 128, 0, 512), C(0, 128, 512, -1)]
+    assert [bench.call_cta_tiles(fh, c) for c in shares] == [16 * 4 * 2, 16 * 4 * 2]
+    assert bench.pick_call_sms(fh, shares, 152) == 76
+    assert bench.pick_call_sms(fh, shares, 100) == 0   # 128 CTA-tiles no longer fit in one wave
+    assert bench.pick_call_sms(fh, shares[:1], 152) == 0
     cp = W.cp_long()                          # 8 shares of 8,192 tokens: 2,048 CTA-tiles each
-    cp_calls = [(0, 128, i * 8192, (i + 1) * 8192, f"out{i}", None) for i in range(8)]
-    assert Step.pick_call_sms(_fake_step(cp, cp_calls), 152) == 0
+    cp_calls = bench.step_pattern(cp)[0][1]
+    assert bench.pick_call_sms(cp, cp_calls, 152) == 0
     hs = W.head_shard()                       # 16-head shards: one head group per call
-    hs_calls = [(i * 16, (i + 1) * 16, 0, -1, f"out{i}", None) for i in range(8)]
-    assert Step.call_cta_tiles(_fake_step(hs, hs_calls), hs_calls[0]) == 128 * 32
+    assert bench.call_cta_tiles(hs, C(0, 16)) == 128 * 32
+    rh = W.ragged_handoff()
+    post = bench.step_pattern(rh, list(range(64)))[2][1]
+    assert bench.pick_call_sms(rh, post, 152) == 0     # the rerun calls are large
 
 
 def test_per_request_ranges_count_their_own_tiles():
-    sys.path.insert(0, ROOT)
-    import bench
+    bench = _bench()
     import torch
     from layout_agnostic_paged_gb300 import workloads as W
     w = W.Workload("ragged shares", (300, 1000, 0), 128, 64, seed=1, token_splits=2,
                    per_request_splits=True)
-    calls = [(0, 128, 0, -1, "out0", None), (0, 128, 0, -1, "out1", None)]
+    calls = bench.step_pattern(w)[0][1]
     rng = W.per_request_ranges(w)             # share i of request r: [L_r i / 2, L_r (i + 1) / 2)
-    st = _fake_step(w, calls, rng)
     # share 0: [0,150) -> tiles 0-1, [0,500) -> tiles 0-3, empty;
     # share 1: [150,300) -> tiles 1-2, [500,1000) -> tiles 3-7, empty
-    assert bench.Step.call_cta_tiles(st, calls[0]) == (2 + 4) * 2
-    assert bench.Step.call_cta_tiles(st, calls[1]) == (2 + 5) * 2
+    assert bench.call_cta_tiles(w, calls[0], rng.tolist()) == (2 + 4) * 2
+    assert bench.call_cta_tiles(w, calls[1], rng.tolist()) == (2 + 5) * 2
     assert torch.equal(rng[0, 1], torch.tensor([150, 500, 0], dtype=torch.int32))
+    # the two shares' tokens add up to the batch's
+    assert sum(bench.call_tokens_pages(w, c, rng.tolist())[0] for c in calls) == 1300
+
+
+def test_reference_step_restricted_to_a_sample_matches_the_oracle_per_phase():
+    """The reference arm's step: the workload's phases run by the oracle over a sample of
+    the requests.  On a small ragged handoff batch the rerun output (pool 1 for the
+    remaining requests, pool 2 for the moved ones, after the oracle's page copy) equals
+    the oracle on the original pool."""
+    bench = _bench()
+    import numpy as np
+    import oracle
+    from layout_agnostic_paged_gb300 import workloads as W
+    w = W.Workload("small handoff", (300, 77, 1000, 129), 8, 16, seed=5, migrate_frac=0.5)
+    inp = W.make_workload_inputs(w)
+    mig = W.make_migration(inp, w.migrate_frac, seed=w.seed)
+    ph = bench.step_pattern(w, mig.requests)
+    q, pool = oracle.bf16_bits(inp.q), oracle.bf16_bits(inp.pool).copy()
+    bt, ctx = inp.block_table.numpy(), inp.ctx_lens.numpy()
+    pool2 = np.zeros((mig.dst_num_pages,) + pool.shape[1:], dtype=np.uint16)
+    bt2 = np.full(bt.shape, -1, dtype=np.int32)
+    bt2[mig.requests] = mig.new_block_table.numpy()
+    out, lse = bench.reference_step(w, ph, q, pool, bt, ctx, np.arange(4), mig, pool2, bt2, None)
+    ro, rl = oracle.decode_attn(q, pool, bt, ctx, w.scale)
+    assert np.allclose(out, ro, rtol=0, atol=1e-12) and np.allclose(lse, rl, rtol=0, atol=1e-12)
 
 
 def _free_port():

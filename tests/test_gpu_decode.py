@@ -161,95 +161,12 @@ def test_workspace_too_small_is_rejected():
         gpu_decode(inp, W.MLA_SCALE, ws=ws[:ws.numel() - 256])
 
 
-# ---------------------------------------------------------------- full-size configs
-
-def test_cp_long_context_workload_sampled():
-    """B=16, ctx 65,536, 128 heads: 8 token shares merged vs the unsplit call, and
-    sampled rows against the oracle."""
-    w = W.cp_long()
-    inp = W.make_workload_inputs(w, device=DEV)
-    B, H = w.batch, w.num_heads
-    span = 65536 // w.token_splits
-    po = torch.empty(w.token_splits, B, H, 512, device=DEV)
-    pl = torch.empty(w.token_splits, B, H, device=DEV)
-    for i in range(w.token_splits):
-        gpu_decode(inp, w.scale, tok_lo=i * span, tok_hi=(i + 1) * span, out=po[i], lse=pl[i])
-    mo = torch.empty(B, H, 512, device=DEV)
-    ml = torch.empty(B, H, device=DEV)
-    S.splash_lse_merge(po, pl, mo, ml)
-    uo, ul, _ = gpu_decode(inp, w.scale)
-    assert_attn_close(mo.cpu(), uo.cpu().double().numpy(), ml.cpu(), ul.cpu().double().numpy(),
-                      "CP merged vs unsplit")
-    for r, h0 in [(0, 0), (7, 61), (15, 125)]:
-        ro, rl = oracle_rows(inp, w.scale, r, h0, h0 + 3)
-        assert_attn_close(uo[r, h0:h0 + 3].cpu(), ro, ul[r, h0:h0 + 3].cpu(), rl, f"cp r{r}")
-        ro, rl = oracle_rows(inp, w.scale, r, h0, h0 + 3, tok_lo=3 * span, tok_hi=4 * span)
-        assert_attn_close(po[3, r, h0:h0 + 3].cpu(), ro, pl[3, r, h0:h0 + 3].cpu(), rl,
-                          f"cp share r{r}")
-
-
-def test_head_shard_workload_sampled():
-    """B=128, ctx 4,096: 8 calls of 16 heads each; concatenation vs sampled oracle rows."""
-    w = W.head_shard()
-    inp = W.make_workload_inputs(w, device=DEV)
-    B, H = w.batch, w.num_heads
-    o = torch.full((B, H, 512), float("nan"), device=DEV)
-    l = torch.full((B, H), float("nan"), device=DEV)
-    ws = None
-    for s in range(w.head_shards):
-        _, _, ws = gpu_decode(inp, w.scale, 16 * s, 16 * s + 16, out=o, lse=l, ws=ws)
-    assert torch.isfinite(o).all() and torch.isfinite(l).all()
-    for r, h0 in [(0, 0), (64, 40), (127, 112)]:
-        ro, rl = oracle_rows(inp, w.scale, r, h0, h0 + 16)
-        assert_attn_close(o[r, h0:h0 + 16].cpu(), ro, l[r, h0:h0 + 16].cpu(), rl, f"shard r{r}")
-
-
-def test_ragged_handoff_workload_sampled():
-    """256 requests, log-uniform 512..131,072: decode, migrate 25% of requests' pages
-    to a second pool (bit-exact), rerun as two calls, compare."""
-    w = W.ragged_handoff()
-    inp = W.make_workload_inputs(w, device=DEV)
-    out, lse, _ = gpu_decode(inp, w.scale)
-    assert torch.isfinite(out).all()
-    B = w.batch
-    lens = list(w.ctx_lens)
-    longest = int(np.argmax(lens))
-    shortest = int(np.argmin(lens))
-    for r in (longest, shortest, 100):
-        ro, rl = oracle_rows(inp, w.scale, r, 0, 4)
-        assert_attn_close(out[r, :4].cpu(), ro, lse[r, :4].cpu(), rl, f"ragged r{r}")
-    m = W.make_migration(inp, w.migrate_frac, seed=w.seed)
-    pool2 = torch.full((m.dst_num_pages, 64, 576), float("nan"), dtype=torch.bfloat16, device=DEV)
-    S.splash_kv_migrate(inp.pool, pool2, m.src_ids.to(DEV), m.dst_ids.to(DEV))
-    torch.cuda.synchronize()
-    src = inp.pool.index_select(0, m.src_ids.to(DEV).long())
-    dst = pool2.index_select(0, m.dst_ids.to(DEV).long())
-    assert torch.equal(src.view(torch.int16), dst.view(torch.int16))
-    moved = torch.tensor(m.requests, device=DEV)
-    keep = torch.tensor([r for r in range(B) if r not in set(m.requests)], device=DEV)
-    inp2 = W.DecodeInputs(q=inp.q[moved].contiguous(), pool=pool2,
-                          block_table=m.new_block_table.to(DEV),
-                          ctx_lens=inp.ctx_lens[moved].contiguous(), perm=inp.perm,
-                          pages_per_req=[inp.pages_per_req[r] for r in m.requests])
-    inp1 = W.DecodeInputs(q=inp.q[keep].contiguous(), pool=inp.pool,
-                          block_table=inp.block_table[keep].contiguous(),
-                          ctx_lens=inp.ctx_lens[keep].contiguous(), perm=inp.perm,
-                          pages_per_req=[inp.pages_per_req[int(r)] for r in keep])
-    o2, l2, _ = gpu_decode(inp2, w.scale)
-    o1, l1, _ = gpu_decode(inp1, w.scale)
-    assert_attn_close(o2.cpu(), out[moved].cpu().double().numpy(), l2.cpu(),
-                      lse[moved].cpu().double().numpy(), "migrated requests")
-    assert_attn_close(o1.cpu(), out[keep].cpu().double().numpy(), l1.cpu(),
-                      lse[keep].cpu().double().numpy(), "remaining requests")
-    r0 = 0
-    ro, rl = oracle_rows(inp2, w.scale, r0, 120, 128)
-    assert_attn_close(o2[r0, 120:].cpu(), ro, l2[r0, 120:].cpu(), rl, "migrated vs oracle")
-
+# ---------------------------------------------------------------- large batches
 
 def test_batch_beyond_the_plans_shared_memory_search():
     """More requests (9,000) than the plan keeps tile ends for in shared memory (8,192):
     the group search then reads the plan from global memory.  Short ragged contexts,
-    some empty; sampled requests against the oracle, and every output finite."""
+    some empty; every request against the oracle."""
     rng = np.random.default_rng(60)
     ctx = [int(x) for x in rng.integers(0, 400, size=9000)]
     inp = W.make_decode_inputs(ctx, 16, 64, seed=60, device=DEV)
@@ -260,30 +177,5 @@ def test_batch_beyond_the_plans_shared_memory_search():
     assert torch.isfinite(out[nonempty]).all() and torch.isfinite(lse[nonempty]).all()
     empty = [r for r, L in enumerate(ctx) if L == 0]
     assert empty and (out[empty] == 0).all() and torch.isneginf(lse[empty]).all()
-    for r in [nonempty[0], 4095, 8191, 8192, 8193, nonempty[-1]] + list(rng.choice(nonempty, 6)):
-        r = int(r)
-        ro, rl = oracle_rows(inp, W.MLA_SCALE, r, 0, 16)
-        assert_attn_close(out[r].cpu(), ro, lse[r].cpu(), rl, f"request {r} of 9000")
-
-
-@pytest.mark.parametrize("name", ["full_heads", "tiny"])
-def test_benchmark_step_matches_oracle(name):
-    """The step the benchmark times, in its own launch configuration (two share calls
-    on two streams, each on half the SMs, then the merge and the handoff's page
-    migration), against the unsplit fp64 oracle and bit-exact pages."""
-    import os
-    import sys
-    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
-    import bench
-    w = W.ALL[name]()
-    inp = W.make_workload_inputs(w, device=DEV)
-    step = bench.Step(w, inp, DEV)
-    assert step.call_sms == torch.cuda.get_device_properties(0).multi_processor_count // 2
-    step.run()
-    torch.cuda.synchronize()
-    assert S.splash_workspace_status(step.ws) == 0 and S.splash_workspace_status(step.ws_b) == 0
-    ro, rl = oracle_full(inp, w.scale)
-    assert_attn_close(step.out.cpu(), ro, step.lse.cpu(), rl, f"{name} benchmark step")
-    src = inp.pool.index_select(0, step.src_ids.long())
-    dst = step.pool2.index_select(0, step.dst_ids.long())
-    assert torch.equal(src.view(torch.int16), dst.view(torch.int16))
+    ro, rl = oracle_full(inp, W.MLA_SCALE)
+    assert_attn_close(out.cpu(), ro, lse.cpu(), rl, "9000 requests")
