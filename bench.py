@@ -7,7 +7,8 @@ One step = one pass of the workload's hot-path rows over one synthetic batch
 the ragged mixed batch with a layout handoff: 256 requests with log-uniform
 contexts of 512..131,072 tokens, 128 query heads over one shared 576-wide latent
 KV head, page 64, shuffled page ids.  Its step is
-  * one decode call over the whole batch (split plan + tcgen05 decode + combine);
+  * one decode call over the whole batch (tcgen05 decode, which computes its own
+    split plan, + combine of requests cut across CTA groups);
   * the handoff: splash_kv_migrate of a seeded 25% of the requests' pages into a
     second block pool at fresh page ids (their block-table rows are rewritten on
     the host, once: an input of the step);
@@ -480,7 +481,9 @@ class Step:
                 s = pick_call_sms(w, ph[1], sms, self.ranges_host) if call_sms < 0 else call_sms
                 for c in ph[1]:
                     self.call_sms[id(c)] = s
-        self.launches_per_step = sum(3 * len(ph[1]) if ph[0] == "decode" else 1
+        # a decode call launches the decode kernel (which computes its own split plan)
+        # and the combine kernel
+        self.launches_per_step = sum(2 * len(ph[1]) if ph[0] == "decode" else 1
                                      for ph in self.phases)
 
     def decode_calls(self):
@@ -757,7 +760,7 @@ def run_ours(args, world, rank, local):
     value = total_tokens * K / (total_ms / 1e3)
     e2e_value = total_tokens * K / (e2e_total / 1e3)
 
-    # roofline of the dominant kernel, the decode call (plan + tcgen05 decode + combine):
+    # roofline of the dominant kernel, the decode call (tcgen05 decode + combine):
     # the algorithmic bytes of every decode call of the step / the decode phases' time
     hbm_peak, bf16_peak, peak_src = measured_peaks()
     dec_idx = [i for i, ph in enumerate(step.phases) if ph[0] == "decode"]
@@ -813,7 +816,7 @@ def run_ours(args, world, rank, local):
             "gpu_launches": step.launches_per_step * K,
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak,
                          "unit": "GB/s", "frac": achieved_gbs / hbm_peak, "traffic": traffic,
-                         "kernel": "splash_decode_attn call (plan + tcgen05 decode + combine)",
+                         "kernel": "splash_decode_attn call (tcgen05 decode with its split plan + combine)",
                          "alg_bytes_per_step": alg_bytes, "decode_us_per_step": dec_s * 1e6,
                          "decode_calls_per_step": len(calls),
                          "timing": dec_src, "peak_source": f"{peak_src} hbm_gbs",

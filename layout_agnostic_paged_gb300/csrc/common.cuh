@@ -19,12 +19,14 @@ constexpr int kTileTokens = 128; // token tile of every decode kernel (the MMA M
 // Decode workspace layout (all offsets 256-byte aligned):
 //   [0, 256)                PlanHeader
 //   [256, ...)              ReqPlan[B]
-//   group_first_req         int32 [G']: first request with a tile in CTA group j
+//   cta_status              uint32 [sts_cap]: SPLASH_DEVICE_* bits of each decode CTA
+//                           (sts_cap: the device's SM count rounded up to 64, or the
+//                           grid if larger, so the layout does not depend on the grid)
 //   partial_out             fp32 [max_slots][Hs][512]
 //   partial_lse             fp32 [max_slots][Hs]
 // ---------------------------------------------------------------------------
 struct PlanHeader {
-    uint32_t status;       // SPLASH_DEVICE_* bits of the last call
+    uint32_t status;       // SPLASH_DEVICE_* bits of the last call (OR of the CTAs' words)
     int32_t num_groups;    // CTA groups in use (<= G', <= T); the tile sequence is cut in that many ranges
     int64_t total_tiles;   // T: tiles over all requests
     int32_t num_reqs;
@@ -49,17 +51,33 @@ static_assert(sizeof(ReqPlan) == 48, "ReqPlan layout");
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Capacity of the per-CTA status array for a device with `sms` SMs and a grid of `ctas`.
+__host__ __device__ inline int status_capacity(int sms, int ctas) {
+    const int n = sms > ctas ? sms : ctas;
+    return (n + 63) / 64 * 64;
+}
+
 struct WorkspaceLayout {
-    size_t req_off, grp_off, pout_off, plse_off, total;
+    size_t req_off, sts_off, pout_off, plse_off, total;
     int max_slots;
-    __host__ __device__ WorkspaceLayout(int B, int Hs, int num_groups) {
+    __host__ __device__ WorkspaceLayout(int B, int Hs, int num_groups, int sts_cap) {
         max_slots = B + num_groups;
         req_off = 256;
-        grp_off = align256(req_off + sizeof(ReqPlan) * size_t(B));      // int32 [num_groups]
-        pout_off = align256(grp_off + sizeof(int32_t) * size_t(num_groups));
+        sts_off = align256(req_off + sizeof(ReqPlan) * size_t(B));      // uint32 [sts_cap]
+        pout_off = align256(sts_off + sizeof(uint32_t) * size_t(sts_cap));
         plse_off = align256(pout_off + size_t(max_slots) * Hs * kDv * sizeof(float));
         total = align256(plse_off + size_t(max_slots) * Hs * sizeof(float));
     }
+};
+
+// One piece of a CTA group's share of the tile sequence: a request, or the part of it
+// that falls in the group's tile range.
+struct Piece {
+    int r;            // request of the call (plan order)
+    int row;          // its storage row in q / block_table / out / lse
+    int t_lo, t_hi;   // tiles of the request (relative to its first tile)
+    int split;
+    bool valid;
 };
 
 // CTA group j of G' owns tiles [a_j, a_{j+1}) of the T-tile sequence, a_j = floor(j T / G').

@@ -35,6 +35,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "plan.cuh"
 
 namespace splash {
 namespace {
@@ -72,9 +73,12 @@ struct TcConfig {
     static constexpr int kBarOff = kRopeOff + kRopes * kColBlockBytes;
     static constexpr int kNumBars = 2 * kPairs + 2 * kRopes + 7;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    // misc: tmem slot (16 B), abort flag (16 B), m[NPAD], m_new[NPAD], alpha[NPAD], red[4][NPAD]
+    // misc: tmem slot (16 B), abort flag (4 B), CTA status word (4 B), pad, m[NPAD],
+    // m_new[NPAD], alpha[NPAD], red[4][NPAD], then the plan scan's 36 int64
     static constexpr int kMiscBytes = 32 + 7 * NPAD * 4;
-    static constexpr int kSmemBytes = kMiscOff + kMiscBytes + 1024;  // + alignment slack
+    static constexpr int kPlanScratchOff = kMiscBytes;
+    static constexpr int kPlanScratchBytes = 36 * 8;
+    static constexpr int kSmemBytes = kMiscOff + kMiscBytes + kPlanScratchBytes + 1024;  // + alignment slack
     static constexpr int kTmemCols = NPAD == 16 ? 128 : (NPAD == 32 ? 256 : 512);
     static constexpr int kOCol = 0;
     static constexpr int kSCol = 4 * NPAD;
@@ -88,43 +92,6 @@ struct TcParams {
     int keep_kv;         // KV loads marked evict-last (a call whose cache fits in L2)
     int group_heads;     // Gs: heads per head group (the last group may have fewer)
     int head_groups;     // NG
-};
-
-struct Piece {
-    int r;            // request of the call (plan order)
-    int row;          // its storage row in q / block_table / out / lse
-    int t_lo, t_hi;   // tiles of the request (relative to its first tile)
-    int split;
-    bool valid;
-};
-
-// Iterates the pieces (request, tile range) of CTA group j, identically in every role.
-struct PieceIter {
-    const ReqPlan* req;
-    int B;
-    int64_t aj, bj;
-    int r;
-    int j;
-    __device__ PieceIter(const ReqPlan* req_, const int32_t* first_req, int B_, int64_t aj_,
-                         int64_t bj_, int j_)
-        : req(req_), B(B_), aj(aj_), bj(bj_), j(j_) {
-        r = (aj < bj) ? first_req[j] : B;
-    }
-    __device__ bool next(Piece& pc, ReqPlan& p) {
-        while (r < B && req[r].tile_begin < bj) {
-            p = req[r];
-            const int cur = r++;
-            if (p.ntiles == 0) continue;
-            pc.r = cur;
-            pc.row = p.row;
-            pc.t_lo = int(max(aj, p.tile_begin) - p.tile_begin);
-            pc.t_hi = int(min(bj, p.tile_begin + p.ntiles) - p.tile_begin);
-            pc.split = j - p.first_grp;
-            pc.valid = true;
-            return true;
-        }
-        return false;
-    }
 };
 
 // Optional phase trace (compiled in only with -DSPLASH_TRACE): globaltimer stamps
@@ -219,6 +186,8 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
     uint8_t* misc = smem + C::kMiscOff;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 16);
+    uint32_t* cta_status_smem = reinterpret_cast<uint32_t*>(misc + 20);
+    int64_t* plan_scratch = reinterpret_cast<int64_t*>(misc + C::kPlanScratchOff);
     float* sm_m = reinterpret_cast<float*>(misc + 32);
     float* sm_mnew = sm_m + NPAD;
     float* sm_alpha = sm_mnew + NPAD;
@@ -227,11 +196,11 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
     const DecodeArgs& a = prm.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
-    PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
-    uint32_t* status = &hdr->status;
-    const WorkspaceLayout lay(a.B, a.Hs, a.num_groups);
-    const ReqPlan* req = reinterpret_cast<const ReqPlan*>(ws + lay.req_off);
-    const int32_t* first_req = reinterpret_cast<const int32_t*>(ws + lay.grp_off);
+    const WorkspaceLayout lay(a.B, a.Hs, a.num_groups, a.sts_cap);
+    // this CTA's status bits collect in shared memory and go to its own workspace word at
+    // the end (the combine kernel ORs the words into the header: no word is shared, so
+    // none needs clearing before the call)
+    uint32_t* status = cta_status_smem;
     const int NG = prm.head_groups;
     const int j = blockIdx.x / NG, g = blockIdx.x % NG;
     const int hbase = g * prm.group_heads;                  // first head of the group in the slice
@@ -261,6 +230,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
         mbar_init(o_free, kSoftmaxThreads * C::kSoftmaxGroups);
         mbar_init(drain, 1);
         *abort_flag = 0;
+        *cta_status_smem = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -277,10 +247,13 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (threadIdx.x == 0) TRACE(1);
-    pdl_wait();     // the plan (and every earlier kernel on the stream) is complete
+    pdl_wait();     // every earlier kernel on the stream is complete (inputs are final)
     if (threadIdx.x == 0) TRACE(2);
-    const int64_t T = hdr->total_tiles;
-    const int G = hdr->num_groups;  // groups in use (<= a.num_groups, <= T)
+    // the split plan: every CTA scans the requests; CTA 0 also writes the request plans
+    // and the header into the workspace
+    const PlanStart plan = plan_prologue(a, j, blockIdx.x == 0, C::kThreads, plan_scratch, status);
+    const int64_t T = plan.T;
+    const int64_t G = plan.G;       // groups in use (<= a.num_groups, <= T)
     const int64_t aj = (T > 0 && j < G) ? group_start(j, T, G) : 0;
     const int64_t bj = (T > 0 && j < G) ? group_start(j + 1, T, G) : 0;
 
@@ -298,7 +271,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
             const uint64_t pol_kv = prm.keep_kv ? policy_evict_last() : policy_evict_first();
             const uint64_t pol_q = policy_evict_last();
             int ps = 0, pph = 0, rs = 0, rph = 0, qph = 0;
-            PieceIter it(req, first_req, a.B, aj, bj, j);
+            PieceIter it(a, plan, aj, bj, j);
             Piece pc;
             ReqPlan p;
             bool ok = true;
@@ -392,7 +365,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
             const uint64_t dv0 = smem_desc(smem_u32(sPair), kColBlockBytes, 1024, 2); // V^T, MN-major
             const uint64_t dp0 = smem_desc(smem_u32(sRope), 1024, 1024, 2);          // P^T, MN-major
             int ps = 0, pph = 0, rs = 0, rph = 0, qph = 0, pfph = 0, ofph = 0;
-            PieceIter it(req, first_req, a.B, aj, bj, j);
+            PieceIter it(a, plan, aj, bj, j);
             Piece pc;
             ReqPlan p;
             bool ok = true;
@@ -499,7 +472,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
         float* plse = reinterpret_cast<float*>(ws + lay.plse_off);
         int sph = 0, ofl = 0, rs = 0;
         int ps_base = 0;      // pair slot of the tile's pair 0 (mirrors the MMA ring)
-        PieceIter it(req, first_req, a.B, aj, bj, j);
+        PieceIter it(a, plan, aj, bj, j);
         Piece pc;
         ReqPlan p;
         bool ok = aj < bj;
@@ -701,6 +674,8 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
     pdl_trigger();
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0)
+        reinterpret_cast<uint32_t*>(ws + lay.sts_off)[blockIdx.x] = *cta_status_smem;
     if (threadIdx.x == 0) TRACE(42);
     if (warp == 1) {
         tc_fence_after();

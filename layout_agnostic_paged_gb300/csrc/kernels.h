@@ -27,15 +27,24 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Arguments of one decode-kernel launch (device pointers, already validated).
 struct DecodeArgs {
-    const void* q;              // bf16 [B][H][576]
+    const void* q;              // bf16 [num_rows][H][576]
     const void* kv_pool;        // bf16 [num_pages][kv_heads][P][576]
-    const int32_t* block_table; // [B][max_pages]
-    float* out;                 // [B][H][512]
-    float* lse;                 // [B][H]
-    void* ws;                   // workspace (plan + partials)
+    const int32_t* block_table; // [num_rows][max_pages]
+    const int32_t* ctx_lens;    // [num_rows]
+    const int32_t* lo_arr;      // [B] per-request token range starts, or null (tok_lo)
+    const int32_t* hi_arr;      // [B] per-request token range ends, or null (tok_hi)
+    const int32_t* rows;        // [B] storage row of request r, or null (row r)
+    float* out;                 // [num_rows][H][512]
+    float* lse;                 // [num_rows][H]
+    void* ws;                   // workspace (plan + per-CTA status + partials)
+    int64_t tok_lo, tok_hi;     // the call's scalar token range (tok_hi < 0: to the end)
     int B, H, P, num_pages, max_pages;
+    int num_rows;               // rows of q / block_table / ctx_lens / out / lse
+    int max_ctx;                // max_pages * P: longest valid context
     int head_lo, Hs;            // head slice
     int num_groups;             // CTA groups G'
+    int ctas;                   // CTAs of the decode grid (num_groups x head groups)
+    int sts_cap;                // capacity of the workspace's per-CTA status array
     int kv_heads;               // KV heads per token (1: the shared latent head)
     int q_per_kv;               // query heads per KV head (H / kv_heads)
     float scale;
@@ -44,14 +53,10 @@ struct DecodeArgs {
 // Raises a kernel's dynamic shared-memory limit once per (kernel, device).
 cudaError_t ensure_smem_optin(const void* kernel, int bytes);
 
-// lo_arr / hi_arr (per-request token ranges) and rows (storage row of each request,
-// of num_rows) may be null: then the scalar range applies and request r is row r.
-cudaError_t launch_plan(const int32_t* ctx_lens, int B, int64_t tok_lo, int64_t tok_hi,
-                        const int32_t* lo_arr, const int32_t* hi_arr, const int32_t* rows,
-                        int num_rows, int max_ctx, int num_groups, int Hs, void* ws,
-                        cudaStream_t stream);
+// K3: merges the partials of requests cut across CTA groups, writes the empty-set
+// result of empty requests and ORs the decode CTAs' status words into the header.
 cudaError_t launch_combine(const void* ws, int B, int H, int head_lo, int Hs, int num_groups,
-                           float* out, float* lse, cudaStream_t stream);
+                           int ctas, int sts_cap, float* out, float* lse, cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* part_out, const float* part_lse, int S, int64_t rows,
                              int d_v, float* out, float* lse, cudaStream_t stream);
 cudaError_t launch_kv_migrate(const void* src, void* dst, size_t page_bytes, const int32_t* src_ids,

@@ -1,18 +1,10 @@
-// plan_merge.cu -- split-KV plan (K1), intra-call combine of split partials (K3)
-// and the public log-sum-exp merge (K4).
-//
-// The plan balances ragged requests across the persistent decode grid: all
-// requests' 128-token tiles are concatenated and cut into at most G' near-equal
-// ranges, one per CTA group (fewer when a range would hold only a few tiles); a
-// request cut across several groups yields one partial per group, combined by K3
-// with the same log-sum-exp merge K4 exposes.  The cut
-// depends only on the context lengths and the token range, never on physical
-// page ids, so results are identical under any page permutation.
+// plan_merge.cu -- intra-call combine of split partials (K3) and the public
+// log-sum-exp merge (K4).  The split plan (K1) that decides which requests are cut
+// across CTA groups is computed by the decode kernel itself (plan.cuh).
 //
 // Method context: "SPLASH: Switching Parallel Layouts of Attention with Seamless
-// Handoff for LLM Serving", Appendix, Table 2 (busiest-rank load of each layout:
-// balance is what the layouts trade; CP reads an equal token share under ideal
-// token partitioning, which is the partial + log-sum-exp merge implemented here).
+// Handoff for LLM Serving", Appendix, Table 2 (CP reads an equal token share under
+// ideal token partitioning; its partials merge by their log-sum-exp weights).
 #include <math.h>
 
 #include "common.cuh"
@@ -22,218 +14,16 @@ namespace splash {
 
 namespace {
 
-constexpr int kPlanThreads = 256;
-
 // Optional kernel-boundary trace (compiled in only with -DSPLASH_TRACE): globaltimer
-// stamps of the plan and combine kernels, read back with splash_ktrace_read().
+// stamps of the combine kernel, read back with splash_ktrace_read().
 #ifdef SPLASH_TRACE
 __device__ unsigned long long g_ktrace[8];
-#define KTRACE_SET(slot) (g_ktrace[slot] = globaltimer_ns())
 #define KTRACE_MIN(slot) atomicMin(&g_ktrace[slot], globaltimer_ns())
 #define KTRACE_MAX(slot) atomicMax(&g_ktrace[slot], globaltimer_ns())
 #else
-#define KTRACE_SET(slot) ((void)0)
 #define KTRACE_MIN(slot) ((void)0)
 #define KTRACE_MAX(slot) ((void)0)
 #endif
-
-// Inclusive block scan of one int64 per thread (kPlanThreads threads).
-__device__ int64_t block_inclusive_scan(int64_t v, int64_t* warp_sums) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int64_t n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
-    }
-    if (lane == 31) warp_sums[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        int64_t s = lane < kPlanThreads / 32 ? warp_sums[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int64_t n = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += n;
-        }
-        warp_sums[lane] = s;
-    }
-    __syncthreads();
-    int64_t add = warp > 0 ? warp_sums[warp - 1] : 0;
-    __syncthreads();
-    return v + add;
-}
-
-// Clipped token range and tile span of one request (the plan's per-request part
-// that depends on nothing but its context length).
-__device__ __forceinline__ ReqPlan request_span(int L, int64_t tok_lo, int64_t tok_hi) {
-    const int64_t lo = tok_lo;
-    const int64_t hi = tok_hi < 0 ? int64_t(L) : min(tok_hi, int64_t(L));
-    ReqPlan p;
-    p.ctx_len = L;
-    if (hi <= lo) {
-        p.lo = p.hi = 0;
-        p.tile0 = 0;
-        p.ntiles = 0;
-    } else {
-        p.lo = int32_t(lo);
-        p.hi = int32_t(hi);
-        p.tile0 = int32_t(lo / kTileTokens);
-        p.ntiles = int32_t((hi + kTileTokens - 1) / kTileTokens - lo / kTileTokens);
-    }
-    p.tile_begin = 0;
-    p.first_grp = 0;
-    p.nsplit = 0;
-    p.slot_base = -1;
-    p.row = -1;
-    p.pad = 0;
-    return p;
-}
-
-// Largest tiles-per-group count for which the plan uses fewer CTA groups than it may.
-constexpr int64_t kRegroupMaxTiles = 4;
-
-// Requests whose tile ends the plan keeps in shared memory for the group search;
-// larger batches search the plan in global memory.
-constexpr int kPlanSmemReqs = 8192;
-
-// One CTA.  Every thread owns a contiguous run of requests; the run is recomputed
-// from the inputs in each pass so that nothing written to global memory is read
-// back, and the group search runs over shared memory.
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ ctx_lens,
-                                                            int B, int64_t tok_lo, int64_t tok_hi,
-                                                            const int32_t* __restrict__ lo_arr,
-                                                            const int32_t* __restrict__ hi_arr,
-                                                            const int32_t* __restrict__ rows,
-                                                            int num_rows, int max_ctx, int num_groups,
-                                                            int Hs, uint8_t* __restrict__ ws) {
-    extern __shared__ int64_t s_end[];  // [B] tile ends, when B <= kPlanSmemReqs
-    __shared__ int64_t warp_sums[32];
-    __shared__ int64_t s_total;
-    if (threadIdx.x == 0) KTRACE_SET(0);
-    pdl_wait();
-    pdl_trigger();  // the decode grid may start its prologue now
-    if (threadIdx.x == 0) KTRACE_SET(1);
-    PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
-    const WorkspaceLayout lay(B, Hs, num_groups);
-    ReqPlan* req = reinterpret_cast<ReqPlan*>(ws + lay.req_off);
-    const bool smem_ends = B <= kPlanSmemReqs;
-
-    const int per = (B + kPlanThreads - 1) / kPlanThreads;
-    const int r0 = min(B, int(threadIdx.x) * per);
-    const int r1 = min(B, r0 + per);
-    // Request r of the call: its storage row (rows[r], else r), its context length and
-    // its token range (lo_arr[r] / hi_arr[r], else the call's scalars), clipped.  A row
-    // outside [0, num_rows), a length outside [0, max_ctx] or a negative range start is
-    // bad input (flagged; the row is skipped, the length clamped, the start taken as 0).
-    auto span_of = [&](int r, bool& bad) {
-        int row = rows ? rows[r] : r;
-        int L = 0;
-        if (row < 0 || row >= num_rows) {
-            bad = true;
-            row = -1;
-        } else {
-            L = ctx_lens[row];
-            if (L < 0 || L > max_ctx) {
-                bad = true;
-                L = min(max(L, 0), max_ctx);
-            }
-        }
-        int64_t lo = tok_lo, hi = tok_hi;
-        if (lo_arr) {
-            lo = lo_arr[r];
-            if (lo < 0) {
-                bad = true;
-                lo = 0;
-            }
-        }
-        if (hi_arr) hi = hi_arr[r];
-        ReqPlan p = request_span(L, lo, hi);
-        if (row < 0) p = request_span(0, 0, 0);
-        p.row = row;
-        return p;
-    };
-
-    // Pass 1: tile counts.
-    bool bad = false;
-    int64_t my_tiles = 0;
-    for (int r = r0; r < r1; ++r) my_tiles += span_of(r, bad).ntiles;
-    const int64_t incl = block_inclusive_scan(my_tiles, warp_sums);
-    if (threadIdx.x == kPlanThreads - 1) s_total = incl;
-    __syncthreads();
-    const int64_t T = s_total;
-    // The busiest group gets k = ceil(T / num_groups) tiles whatever the cut.  When k is
-    // small, ceil(T / k) groups keep that critical path while giving every group k or
-    // k - 1 tiles: fewer requests are split (fewer partial rows to merge) and the spare
-    // SMs are free for concurrent work.  For long runs of tiles the extra tile on the
-    // average group costs more than it saves, so every group is used.  G <= T makes
-    // every group range non-empty, so a request's pieces are exactly the groups its
-    // tiles fall in.
-    const int64_t k = T > 0 ? (T + num_groups - 1) / num_groups : 0;
-    const int64_t G = k == 0 ? 0 : k <= kRegroupMaxTiles ? (T + k - 1) / k : min(int64_t(num_groups), T);
-
-    // Pass 2: global tile offsets, CTA-group cut and partial-slot counts.
-    int64_t my_slots = 0;
-    {
-        int64_t tb = incl - my_tiles;
-        bool unused = false;
-        for (int r = r0; r < r1; ++r) {
-            const ReqPlan p = span_of(r, unused);
-            if (p.ntiles > 0) {
-                const int64_t nsplit = group_of_tile(tb + p.ntiles - 1, T, G) - group_of_tile(tb, T, G) + 1;
-                if (nsplit > 1) my_slots += nsplit;
-            }
-            tb += p.ntiles;
-        }
-    }
-    const int64_t sincl = block_inclusive_scan(my_slots, warp_sums);
-
-    // Pass 3: the complete request plans.
-    {
-        int64_t tb = incl - my_tiles, slot = sincl - my_slots;
-        bool unused = false;
-        for (int r = r0; r < r1; ++r) {
-            ReqPlan p = span_of(r, unused);
-            p.tile_begin = tb;
-            if (p.ntiles > 0) {
-                const int64_t g0 = group_of_tile(tb, T, G);
-                const int64_t g1 = group_of_tile(tb + p.ntiles - 1, T, G);
-                p.first_grp = int32_t(g0);
-                p.nsplit = int32_t(g1 - g0 + 1);
-                if (p.nsplit > 1) {
-                    p.slot_base = int32_t(slot);
-                    slot += p.nsplit;
-                }
-            }
-            req[r] = p;
-            tb += p.ntiles;
-            if (smem_ends) s_end[r] = tb;
-        }
-    }
-    const bool any_bad = __syncthreads_or(bad);  // also publishes s_end
-    // First request of every CTA group: smallest r whose tiles reach past the group start,
-    // so a decode CTA finds its first piece with one load instead of a search.
-    int32_t* first_req = reinterpret_cast<int32_t*>(ws + lay.grp_off);
-    for (int64_t j = threadIdx.x; j < G; j += kPlanThreads) {
-        const int64_t x = group_start(j, T, G);
-        int lo = 0, hi = B;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            const int64_t end = smem_ends ? s_end[mid] : req[mid].tile_begin + req[mid].ntiles;
-            if (end > x) hi = mid;
-            else lo = mid + 1;
-        }
-        first_req[j] = lo;
-    }
-    if (threadIdx.x == kPlanThreads - 1) {
-        hdr->status = any_bad ? uint32_t(SPLASH_DEVICE_BAD_INPUT) : 0u;
-        hdr->num_groups = int32_t(G);
-        hdr->total_tiles = T;
-        hdr->num_reqs = B;
-        hdr->heads = Hs;
-        hdr->max_slots = lay.max_slots;
-        hdr->slots_used = int32_t(sincl);
-        KTRACE_SET(2);
-    }
-}
 
 // Merge `S` partial rows (out at stride `ostride` floats, lse at stride `lstride`)
 // into one output row; one warp.  Lane s < 32 owns split s's weight (broadcast by
@@ -356,19 +146,28 @@ __device__ __forceinline__ void warp_lse_merge(const float* __restrict__ pout, i
 
 // K3: one warp per (request, head) of the call's slice.  Requests cut across
 // several CTA groups are merged from the workspace; empty requests get the
-// empty-set result; single-piece requests were written by the decode kernel.
-__global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict__ ws, int B, int H,
-                                                      int head_lo, int Hs, int num_groups,
-                                                      float* __restrict__ out,
+// empty-set result; single-piece requests were written by the decode kernel.  The
+// first warp also ORs the decode CTAs' status words into the header.
+__global__ void __launch_bounds__(256) combine_kernel(uint8_t* __restrict__ ws, int B, int H,
+                                                      int head_lo, int Hs, int num_groups, int ctas,
+                                                      int sts_cap, float* __restrict__ out,
                                                       float* __restrict__ lse) {
     if (threadIdx.x == 0) KTRACE_MIN(3);
     pdl_wait();
     if (threadIdx.x == 0) KTRACE_MIN(4);
     if (threadIdx.x == 0) KTRACE_MAX(5);
+    const WorkspaceLayout lay(B, Hs, num_groups, sts_cap);
+    if (blockIdx.x == 0 && threadIdx.x < 32) {
+        const uint32_t* sts = reinterpret_cast<const uint32_t*>(ws + lay.sts_off);
+        uint32_t bits = 0;
+        for (int i = threadIdx.x; i < ctas; i += 32) bits |= sts[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
+        if (threadIdx.x == 0) reinterpret_cast<PlanHeader*>(ws)->status = bits;
+    }
     const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (row >= int64_t(B) * Hs) return;
     const int r = int(row / Hs), hh = int(row % Hs);
-    const WorkspaceLayout lay(B, Hs, num_groups);
     const ReqPlan p = reinterpret_cast<const ReqPlan*>(ws + lay.req_off)[r];
     if (p.nsplit == 1 || p.row < 0) return;
     float* o = out + (int64_t(p.row) * H + head_lo + hh) * kDv;
@@ -412,27 +211,14 @@ extern "C" __attribute__((visibility("default"))) int splash_ktrace_clear() {
 }
 #endif
 
-cudaError_t launch_plan(const int32_t* ctx_lens, int B, int64_t tok_lo, int64_t tok_hi,
-                        const int32_t* lo_arr, const int32_t* hi_arr, const int32_t* rows,
-                        int num_rows, int max_ctx, int num_groups, int Hs, void* ws,
-                        cudaStream_t stream) {
-    const int smem = B <= kPlanSmemReqs ? B * int(sizeof(int64_t)) : 0;
-    if (smem > 48 * 1024) {
-        cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(plan_kernel), smem);
-        if (e != cudaSuccess) return e;
-    }
-    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), size_t(smem), stream, ctx_lens, B,
-                      tok_lo, tok_hi, lo_arr, hi_arr, rows, num_rows, max_ctx, num_groups, Hs,
-                      static_cast<uint8_t*>(ws));
-}
-
 cudaError_t launch_combine(const void* ws, int B, int H, int head_lo, int Hs, int num_groups,
-                           float* out, float* lse, cudaStream_t stream) {
+                           int ctas, int sts_cap, float* out, float* lse, cudaStream_t stream) {
     const int64_t threads = int64_t(B) * Hs * 32;
     const int blocks = int((threads + 255) / 256);
     if (blocks == 0) return cudaSuccess;
     return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, stream,
-                      static_cast<const uint8_t*>(ws), B, H, head_lo, Hs, num_groups, out, lse);
+                      static_cast<uint8_t*>(const_cast<void*>(ws)), B, H, head_lo, Hs, num_groups,
+                      ctas, sts_cap, out, lse);
 }
 
 cudaError_t launch_lse_merge(const float* part_out, const float* part_lse, int S, int64_t rows,

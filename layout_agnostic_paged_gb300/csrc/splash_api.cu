@@ -146,7 +146,8 @@ size_t splash_decode_workspace_size(const splash_attn_desc* desc, int head_lo, i
     if (sms <= 0) return 0;
     const int Hs = head_hi - head_lo;
     const Geometry g = decode_geometry(Hs, sms);
-    return WorkspaceLayout(desc->num_reqs, Hs, g.num_groups).total;
+    return WorkspaceLayout(desc->num_reqs, Hs, g.num_groups,
+                           status_capacity(sms, g.num_groups * g.head_groups)).total;
 }
 
 int splash_decode_attn(const splash_attn_desc* desc, const void* q, const void* kv_pool,
@@ -204,30 +205,38 @@ int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext*
     const int Hs = head_hi - head_lo;
     const Geometry g = decode_geometry(Hs, max_sms > 0 && max_sms < sms ? max_sms : sms,
                                        kv_group_heads);
-    const WorkspaceLayout lay(B, Hs, g.num_groups);
+    const int ctas = g.num_groups * g.head_groups;
+    const int sts_cap = status_capacity(sms, ctas);
+    const WorkspaceLayout lay(B, Hs, g.num_groups, sts_cap);
     if (ws_bytes < lay.total) return SPLASH_ERR_WORKSPACE;
     if (B == 0) return SPLASH_OK;
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    const int max_ctx = desc->max_pages_per_req * desc->page_size;
-    if (launch_plan(ctx_lens, B, tok_lo, tok_hi, lo_arr, hi_arr, rows, num_rows, max_ctx,
-                    g.num_groups, Hs, workspace, stream) != cudaSuccess)
-        return SPLASH_ERR_CUDA;
     DecodeArgs a;
     a.q = q;
     a.kv_pool = kv_pool;
     a.block_table = block_table;
+    a.ctx_lens = ctx_lens;
+    a.lo_arr = lo_arr;
+    a.hi_arr = hi_arr;
+    a.rows = rows;
     a.out = out;
     a.lse = lse;
     a.ws = workspace;
+    a.tok_lo = tok_lo;
+    a.tok_hi = tok_hi;
     a.B = B;
     a.H = desc->num_heads;
     a.P = desc->page_size;
     a.num_pages = desc->num_pages;
     a.max_pages = desc->max_pages_per_req;
+    a.num_rows = num_rows;
+    a.max_ctx = desc->max_pages_per_req * desc->page_size;
     a.head_lo = head_lo;
     a.Hs = Hs;
     a.num_groups = g.num_groups;
+    a.ctas = ctas;
+    a.sts_cap = sts_cap;
     a.kv_heads = kv_heads;
     a.q_per_kv = desc->num_heads / kv_heads;
     a.scale = desc->scale;
@@ -245,8 +254,8 @@ int splash_decode_attn_ex(const splash_attn_desc* desc, const splash_decode_ext*
         if (launch_decode_tc(a, mq, mkv, g.head_groups, g.group_heads, stream) != cudaSuccess)
             return SPLASH_ERR_CUDA;
     }
-    if (launch_combine(workspace, B, desc->num_heads, head_lo, Hs, g.num_groups, out, lse, stream) !=
-        cudaSuccess)
+    if (launch_combine(workspace, B, desc->num_heads, head_lo, Hs, g.num_groups, ctas, sts_cap, out,
+                       lse, stream) != cudaSuccess)
         return SPLASH_ERR_CUDA;
     return SPLASH_OK;
 }

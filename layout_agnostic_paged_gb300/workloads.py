@@ -96,6 +96,15 @@ def ragged_handoff() -> Workload:
                     migrate_frac=0.25)
 
 
+def ragged_small() -> Workload:
+    """The ragged + handoff batch scaled to 64 requests (same length distribution): a
+    pool of a few GB, small enough for multi-pass profiler captures of one decode call."""
+    return Workload("ragged mixed batch + handoff, scaled: 64 requests, ctx log-uniform "
+                    "512..131072, 128 heads, page 64, migrate 25%",
+                    ragged_ctx_lens(64, 512, 131072, seed=1007), 128, 64, seed=1007,
+                    migrate_frac=0.25)
+
+
 def ragged_cp() -> Workload:
     return Workload("ragged CP: 128 requests, ctx log-uniform 512..131072, 128 heads, page 64, "
                     "8 token shares of each request's own length",
@@ -117,7 +126,8 @@ def per_request_ranges(w: Workload) -> torch.Tensor:
 
 
 ALL = {"tiny": tiny, "full_heads": full_heads, "cp_long": cp_long, "head_shard": head_shard,
-       "ragged_handoff": ragged_handoff, "ragged_cp": ragged_cp, "gqa": gqa}
+       "ragged_handoff": ragged_handoff, "ragged_small": ragged_small, "ragged_cp": ragged_cp,
+       "gqa": gqa}
 
 
 @dataclass
