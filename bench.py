@@ -85,15 +85,18 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("decode_tc.cu", "common.cuh"):
+    for name in ("decode_tc.cu", "common.cuh", "plan.cuh"):
         with open(os.path.join(ROOT, "layout_agnostic_paged_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+def ncu_traffic(workload: str, alg_bytes_per_step: float):
+    """DRAM bytes of the step's decode launches from the committed ncu summary, if it
+    was taken on the current kernel source (else None).  An entry either gives the bytes
+    of the workload's own decode launches in one step (dram_bytes_per_step) or the ratio
+    of DRAM bytes to algorithmic bytes measured on a scaled-down case of the same
+    workload (dram_over_algorithmic), applied to the step's algorithmic bytes."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
@@ -102,7 +105,9 @@ def ncu_traffic(workload: str):
     e = d.get(workload)
     if not e or e.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return float(e["dram_bytes_per_launch"])
+    if "dram_over_algorithmic" in e:
+        return float(e["dram_over_algorithmic"]) * alg_bytes_per_step
+    return float(e["dram_bytes_per_step"])
 
 
 class ClockSampler:
@@ -771,7 +776,7 @@ def run_ours(args, world, rank, local):
     dec_s = sum(ph_us[i] for i in dec_idx) / 1e6
     achieved_gbs = alg_bytes / dec_s / 1e9
     achieved_tfs = alg_flops / dec_s / 1e12
-    traffic = ncu_traffic(args.workload)
+    traffic = ncu_traffic(args.workload, alg_bytes)
     clocks = clk.summary()
     rows_report = {}
     for i, ph in enumerate(step.phases):
