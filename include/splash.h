@@ -124,8 +124,9 @@ SPLASH_API size_t splash_decode_workspace_size(const splash_attn_desc* desc, int
  *               overlap on the device
  * Slot contents of KV pages beyond ctx_len (tail slots, unused pages) may hold
  * any bits, NaN included: they never reach an output.  A block-table id outside
- * [0, num_pages) for a needed page reads as zeros, and a context length outside
- * [0, max_pages_per_req * P] is clamped into it; both set SPLASH_DEVICE_BAD_INPUT.
+ * [0, num_pages) for a needed page is not read: that page's tokens are left out of
+ * T_r.  A context length outside [0, max_pages_per_req * P] is clamped into it.
+ * Both set SPLASH_DEVICE_BAD_INPUT.
  * Returns SPLASH_OK or a splash_status error (nothing enqueued on error).
  */
 SPLASH_API int splash_decode_attn(const splash_attn_desc* desc, const void* q, const void* kv_pool,

@@ -487,12 +487,14 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
             for (int t = pc.t_lo; t < pc.t_hi; ++t) {
                 const bool first = (t == pc.t_lo);
                 const int tok = (p.tile0 + t) * kTileTokens + row;
-                const bool valid = tok >= p.lo && tok < p.hi;
                 bool in_ctx = tok < p.ctx_len;
                 if (in_ctx) {
                     const int id = bt[tok / P];
                     in_ctx = id >= 0 && id < a.num_pages;
                 }
+                // a token of an unreadable page (bad id) is left out of the attention: its
+                // key rows in shared memory are whatever the slot held before
+                const bool valid = tok >= p.lo && tok < p.hi && in_ctx;
                 bool w = mbar_wait(s_full, sph, abort_flag, status);
                 if (named_barrier_or(bar, kSoftmaxThreads, !w)) { ok = false; break; }
                 sph ^= 1;

@@ -146,12 +146,29 @@ def test_unaligned_token_ranges():
         assert_attn_close(out.cpu(), ro, lse.cpu(), rl, f"range [{lo},{hi})")
 
 
-def test_bad_page_id_is_flagged_not_faulted():
-    inp = _inputs([200, 64], 16, 64, seed=28)
-    inp.block_table[0, 1] = 10_000_000
+@pytest.mark.parametrize("H", [128, 16])
+def test_bad_page_ids_are_flagged_and_their_tokens_left_out(H):
+    """A block-table id outside the pool for a needed page is not read: the kernel flags
+    it and leaves that page's tokens out of the attention.  The expectation is the
+    oracle over each request's readable tokens (two token ranges merged by their
+    log-sum-exp weights)."""
+    import oracle
+    inp = _inputs([200, 64, 1000], H, 64, seed=28)
+    good = W.DecodeInputs(q=inp.q, pool=inp.pool, block_table=inp.block_table.clone(),
+                          ctx_lens=inp.ctx_lens, perm=inp.perm, pages_per_req=inp.pages_per_req)
+    inp.block_table[0, 1] = 10_000_000        # tokens [64, 128) of request 0
+    inp.block_table[2, 7] = -5                # tokens [448, 512) of request 2
     out, lse, ws = gpu_decode(inp, W.MLA_SCALE)
     flags = S.splash_workspace_status(ws)
     assert flags & S.SPLASH_DEVICE_BAD_INPUT
+    assert not flags & S.SPLASH_DEVICE_TIMEOUT
+    for r, (b0, b1) in {0: (64, 128), 2: (448, 512)}.items():
+        o0, l0 = oracle_rows(good, W.MLA_SCALE, r, 0, H, tok_lo=0, tok_hi=b0)
+        o1, l1 = oracle_rows(good, W.MLA_SCALE, r, 0, H, tok_lo=b1, tok_hi=-1)
+        mo, ml = oracle.lse_merge(np.stack([o0, o1]), np.stack([l0, l1]))
+        assert_attn_close(out[r].cpu(), mo, lse[r].cpu(), ml, f"request {r} without its bad page")
+    ro, rl = oracle_rows(good, W.MLA_SCALE, 1, 0, H)
+    assert_attn_close(out[1].cpu(), ro, lse[1].cpu(), rl, "request 1 (all pages readable)")
 
 
 def test_workspace_too_small_is_rejected():
