@@ -447,7 +447,12 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                     if (++rs == C::kRopes) { rs = 0; rph ^= 1; }
                 }
             }
-            // drain: every MMA issued so far has completed before TMEM is released
+            // drain: every MMA issued so far has completed before TMEM is released.  The
+            // wait is bounded like every other; if it gives up, the status word already
+            // says SPLASH_DEVICE_TIMEOUT (the call's outputs are invalid) and the CTA still
+            // deallocates at the teardown: an allocation must not outlive its CTA, and a
+            // tensor pipe that has not finished 2 s after its last issue is the fault the
+            // status word reports, not a state the kernel can wait out.
             tc_commit(drain);
             volatile int never = 0;
             mbar_wait(drain, 0, &never, status);
