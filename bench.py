@@ -468,14 +468,16 @@ class Step:
         # with its own workspace (sized for the largest call it runs)
         self.stream_b = torch.cuda.Stream(device)
         need = [0, 0]
-        for ph in self.phases:
-            if ph[0] == "decode":
-                for k, c in enumerate(ph[1]):
-                    nreq = B if c.rows is None else len(c.rows)
-                    ws = S.decode_workspace(inp.q, inp.pool, inp.block_table, w.scale, c.head_lo,
-                                            c.head_hi, num_reqs=nreq)
-                    need[k % 2] = max(need[k % 2], ws.numel())
-                    del ws
+        desc = S.make_desc(inp.q, inp.pool, inp.block_table, w.scale)
+        with torch.cuda.device(device):
+            for ph in self.phases:
+                if ph[0] == "decode":
+                    for k, c in enumerate(ph[1]):
+                        desc.num_reqs = B if c.rows is None else len(c.rows)
+                        n = S.splash_decode_workspace_size(desc, c.head_lo, c.head_hi)
+                        if n == 0:
+                            raise S.SplashError(S.SPLASH_ERR_UNSUPPORTED, "splash_decode_workspace_size")
+                        need[k % 2] = max(need[k % 2], n)
         self.ws = torch.empty(need[0], dtype=torch.uint8, device=device)
         self.ws_b = torch.empty(need[1], dtype=torch.uint8, device=device) if need[1] else None
         sms = torch.cuda.get_device_properties(device).multi_processor_count
