@@ -44,15 +44,16 @@ int splash_decode_attn_noalloc(const splash_attn_desc* desc, const void* q, cons
                                const int32_t* block_table, const int32_t* ctx_lens, int head_lo,
                                int head_hi, int64_t tok_lo, int64_t tok_hi, float* out,
                                float* lse, splash_stream_t stream) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SPLASH_ERR_CUDA;
     const size_t need = splash_decode_workspace_size(desc, head_lo, head_hi);
     if (need == 0) {
-        // invalid or unsupported shape: let the regular entry point report which
+        // invalid or unsupported shape (or no device): let the regular entry point report
+        // which, with the same argument checks in the same order
         return splash_decode_attn(desc, q, kv_pool, block_table, ctx_lens, head_lo, head_hi,
                                   tok_lo, tok_hi, out, lse, nullptr, 0, stream);
     }
     if (need > splash::kNoAllocScratchBytes) return SPLASH_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SPLASH_ERR_CUDA;
     void* scratch = nullptr;
     const int st = splash::scratch_address(dev, &scratch);
     if (st != SPLASH_OK) return st;

@@ -157,6 +157,17 @@ def test_migrate_rejects_bad_arguments(lib):
 def test_status_reader_rejects_null(lib):
     flags = ctypes.c_uint32(0)
     assert lib.splash_workspace_status(None, ctypes.byref(flags), None) == S.SPLASH_ERR_INVALID_ARG
+    assert lib.splash_workspace_status(ctypes.c_void_p(FAKE), None, None) == S.SPLASH_ERR_INVALID_ARG
+    # the no-allocation entry point's status reader checks its output pointer first
+    assert lib.splash_noalloc_status(None, None) == S.SPLASH_ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_invalid_shapes_before_touching_the_scratch(lib):
+    vp = ctypes.c_void_p
+    f = lib.splash_decode_attn_noalloc
+    args = (vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 0, 8, 0, -1, vp(FAKE), vp(FAKE), vp(0))
+    assert f(ctypes.byref(_desc(d_qk=512)), *args) == S.SPLASH_ERR_UNSUPPORTED
+    assert f(ctypes.byref(_desc(num_heads=0)), *args) == S.SPLASH_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_cuda_tensors():
