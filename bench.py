@@ -866,6 +866,10 @@ def cpu_baseline(w, inp, seconds: float):
         t1, toks1, n1 = 0.0, 0, 0
         while t1 < seconds / 4 and n1 < n:
             r = n1 % B
+            # stop before a request that would overrun the budget by half (the time per
+            # token so far predicts it)
+            if toks1 > 0 and t1 + int(ctx[r]) * (t1 / toks1) > 1.5 * seconds / 4:
+                break
             t0 = time.perf_counter()
             oracle.decode_attn(q[r:r + 1], pool, bt[r:r + 1], ctx[r:r + 1], w.scale)
             t1 += time.perf_counter() - t0
