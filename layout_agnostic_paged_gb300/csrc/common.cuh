@@ -303,9 +303,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 // visible (a no-op for an ordinary launch), so every kernel calls it before its
 // first global-memory access.  pdl_trigger() lets the successor start launching.
 // A successor that launches early holds SM slots while it waits, which a kernel on
-// another stream may need: only the plan triggers at once (its successor is the
-// decode grid, whose prologue then overlaps the plan), the decode triggers when its
-// work is done, and the short kernels never (their successors launch as they exit).
+// another stream may need: so the decode triggers only when its work is done, and the
+// short kernels (combine, merge, migration) never trigger (their successors launch as
+// they exit).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

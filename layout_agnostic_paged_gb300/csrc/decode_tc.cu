@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
     // host); page p of that KV head starts at row (p * kv_heads + kvh) * P of the pool
     const int kvh = a.kv_heads > 1 ? (a.head_lo + hbase) / a.q_per_kv : 0;
 
-    // Prologue (overlaps the plan kernel under programmatic dependent launch).
+    // Prologue (overlaps the previous kernel on the stream under programmatic dependent
+    // launch: nothing here reads global memory).
     if (threadIdx.x == 0) TRACE(0);
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kPairs; ++i) {

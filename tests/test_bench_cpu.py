@@ -31,6 +31,25 @@ def test_bench_module_imports_without_gpu():
     assert len(bench.kernel_source_hash()) == 16
 
 
+def test_kernel_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    """The stored ncu counters follow the code: comments and whitespace do not change the
+    hash, a changed token does."""
+    bench = _bench()
+    src = os.path.join(ROOT, "layout_agnostic_paged_gb300", "csrc")
+    dst = tmp_path / "layout_agnostic_paged_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for name in ("decode_tc.cu", "common.cuh", "plan.cuh"):
+        (dst / name).write_text(open(os.path.join(src, name)).read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    f = dst / "decode_tc.cu"
+    text = f.read_text()
+    f.write_text(text.replace("namespace splash {", "// a note\nnamespace   splash /* x */ {", 1))
+    assert bench.kernel_source_hash() == h0
+    f.write_text(text.replace("kTau = 8.0f", "kTau = 9.0f", 1))
+    assert bench.kernel_source_hash() != h0
+
+
 def _bench():
     sys.path.insert(0, ROOT)
     import bench
