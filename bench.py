@@ -353,13 +353,43 @@ def call_cta_tiles(w, c, ranges=None):
     return tiles * -(-(c.head_hi - c.head_lo) // 64)
 
 
+def token_share_phase(calls):
+    """Whether a phase's calls are the token shares of one CP group: the same heads and
+    requests, each call a different share of every request's tokens (scalar ranges that
+    do not overlap, or distinct per-request shares).  Such calls read disjoint KV."""
+    if len(calls) < 3:
+        return False
+    c0 = calls[0]
+    if any(c.head_lo != c0.head_lo or c.head_hi != c0.head_hi or c.rows != c0.rows
+           or c.pool != c0.pool for c in calls):
+        return False
+    if all(c.share is not None for c in calls):
+        return len({c.share for c in calls}) == len(calls)
+    if any(c.share is not None for c in calls):
+        return False
+    spans = sorted((c.tok_lo, c.tok_hi if c.tok_hi >= 0 else math.inf) for c in calls)
+    return all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))
+
+
+def pick_lanes(calls):
+    """Streams a decode phase's calls run on.  The token shares of a CP group run all at
+    once, as the group's ranks would, each call on its own stream; other multi-call
+    phases alternate between two streams."""
+    if token_share_phase(calls):
+        return len(calls)
+    return 2 if len(calls) > 1 else 1
+
+
 def pick_call_sms(w, calls, sms, ranges=None):
-    """A phase of several calls whose tiles each fill at most one wave of the GPU would
-    leave SMs idle while the other stream's call waits for them; such calls each get
-    half the SMs and run side by side (two ranks sharing one GPU).  Larger calls, and a
-    phase of one call, keep every SM."""
+    """SM budget of each call of a phase (0: all).  The concurrent token shares of a CP
+    group split the SMs evenly.  A phase of several calls whose tiles each fill at most
+    one wave of the GPU would leave SMs idle while the other stream's call waits for
+    them; such calls each get half the SMs and run side by side (two ranks sharing one
+    GPU).  Larger calls, and a phase of one call, keep every SM."""
     if len(calls) < 2:
         return 0
+    if token_share_phase(calls):
+        return sms // len(calls)
     if all(call_cta_tiles(w, c, ranges) <= sms for c in calls):
         return sms // 2
     return 0
@@ -471,22 +501,25 @@ class Step:
             self.src_ids = self.mig.src_ids.to(device)
             self.dst_ids = self.mig.dst_ids.to(device)
             self.page_bytes = int(inp.pool[0].numel() * inp.pool.element_size())
-        # calls of a phase alternate between the current stream and a second one, each
-        # with its own workspace (sized for the largest call it runs)
-        self.stream_b = torch.cuda.Stream(device)
-        need = [0, 0]
+        # call k of a decode phase runs on lane k % lanes: lane 0 is the current stream,
+        # the others streams of their own; each lane has its own workspace (sized for the
+        # largest call it runs)
+        self.lanes = [pick_lanes(ph[1]) if ph[0] == "decode" else 1 for ph in self.phases]
+        n_lanes = max(self.lanes)
+        self.streams = [None] + [torch.cuda.Stream(device) for _ in range(n_lanes - 1)]
+        need = [0] * n_lanes
         desc = S.make_desc(inp.q, inp.pool, inp.block_table, w.scale)
         with torch.cuda.device(device):
-            for ph in self.phases:
+            for ph, lanes in zip(self.phases, self.lanes):
                 if ph[0] == "decode":
                     for k, c in enumerate(ph[1]):
                         desc.num_reqs = B if c.rows is None else len(c.rows)
                         n = S.splash_decode_workspace_size(desc, c.head_lo, c.head_hi)
                         if n == 0:
                             raise S.SplashError(S.SPLASH_ERR_UNSUPPORTED, "splash_decode_workspace_size")
-                        need[k % 2] = max(need[k % 2], n)
-        self.ws = torch.empty(need[0], dtype=torch.uint8, device=device)
-        self.ws_b = torch.empty(need[1], dtype=torch.uint8, device=device) if need[1] else None
+                        need[k % lanes] = max(need[k % lanes], n)
+        self.wss = [torch.empty(n, dtype=torch.uint8, device=device) for n in need if n]
+        self.ws = self.wss[0]
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         self.sms = sms
         self.call_sms = {}
@@ -525,20 +558,23 @@ class Step:
         import torch
         if ph[0] == "decode":
             calls = ph[1]
+            lanes = self.lanes[self.phases.index(ph)]
             cur = torch.cuda.current_stream()
-            if len(calls) > 1:
+            if lanes > 1:
                 fork = torch.cuda.Event()
                 fork.record(cur)
-                self.stream_b.wait_event(fork)
+                for st in self.streams[1:lanes]:
+                    st.wait_event(fork)
             for k, c in enumerate(calls):
-                if k % 2:
-                    with torch.cuda.stream(self.stream_b):
-                        self.decode(c, self.ws_b, max_sms)
+                lane = k % lanes
+                if lane:
+                    with torch.cuda.stream(self.streams[lane]):
+                        self.decode(c, self.wss[lane], max_sms)
                 else:
                     self.decode(c, self.ws, max_sms)
-            if len(calls) > 1:
+            for st in self.streams[1:lanes]:
                 join = torch.cuda.Event()
-                join.record(self.stream_b)
+                join.record(st)
                 cur.wait_event(join)
         elif ph[0] == "merge":
             self.S.splash_lse_merge(self.po[:ph[1]], self.pl[:ph[1]], self.out, self.lse)
@@ -743,9 +779,9 @@ def run_ours(args, world, rank, local):
                     "alone + migrate alone",
         }
     total_ms = max_over_ranks(sum(step_ms), world, device)
-    status = S.splash_workspace_status(step.ws)
-    if step.ws_b is not None:
-        status |= S.splash_workspace_status(step.ws_b)
+    status = 0
+    for ws in step.wss:
+        status |= S.splash_workspace_status(ws)
     if status != 0:
         raise RuntimeError(f"device status word set: {status}")
 
@@ -812,12 +848,16 @@ def run_ours(args, world, rank, local):
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(w, inp, args.cpu_seconds)
-        launch = ("calls of a decode phase alternate between two streams, one workspace each"
-                  if any(ph[0] == "decode" and len(ph[1]) > 1 for ph in step.phases) else
-                  "one stream")
+        if any(ph[0] == "decode" and lanes > 2 for ph, lanes in zip(step.phases, step.lanes)):
+            launch = ("the token shares of the CP group run at once, each call on its own stream "
+                      "and workspace")
+        elif any(ph[0] == "decode" and len(ph[1]) > 1 for ph in step.phases):
+            launch = "calls of a decode phase alternate between two streams, one workspace each"
+        else:
+            launch = "one stream"
         small = sorted({s for s in step.call_sms.values() if s})
         if small:
-            launch += f"; calls that fit in one wave limited to {small[0]} of {step.sms} SMs each"
+            launch += f"; each call limited to {small[0]} of {step.sms} SMs"
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": Wm, "ms_per_step": total_ms / K, "higher_is_better": True,

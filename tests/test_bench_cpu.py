@@ -100,14 +100,36 @@ def test_small_two_call_phases_get_half_the_sms():
     assert bench.pick_call_sms(fh, shares, 152) == 76
     assert bench.pick_call_sms(fh, shares, 100) == 0   # 128 CTA-tiles no longer fit in one wave
     assert bench.pick_call_sms(fh, shares[:1], 152) == 0
-    cp = W.cp_long()                          # 8 shares of 8,192 tokens: 2,048 CTA-tiles each
-    cp_calls = bench.step_pattern(cp)[0][1]
-    assert bench.pick_call_sms(cp, cp_calls, 152) == 0
     hs = W.head_shard()                       # 16-head shards: one head group per call
     assert bench.call_cta_tiles(hs, C(0, 16)) == 128 * 32
+    hs_calls = bench.step_pattern(hs)[0][1]
+    assert not bench.token_share_phase(hs_calls)       # same tokens, other heads
+    assert bench.pick_lanes(hs_calls) == 2 and bench.pick_call_sms(hs, hs_calls, 152) == 0
     rh = W.ragged_handoff()
     post = bench.step_pattern(rh, list(range(64)))[2][1]
+    assert not bench.token_share_phase(post)           # other requests
     assert bench.pick_call_sms(rh, post, 152) == 0     # the rerun calls are large
+
+
+def test_cp_token_shares_run_at_once_on_an_even_sm_split():
+    """The 8 token shares of a CP group read disjoint KV: they run as the group's ranks
+    would, all at once, each on its own stream with an eighth of the SMs.  The scalar
+    shares of the long-context batch (the last one open-ended) and the per-request shares
+    of the ragged batch both qualify; overlapping or repeated shares do not."""
+    bench = _bench()
+    from layout_agnostic_paged_gb300 import workloads as W
+    C = bench.CallSpec
+    cp = W.cp_long()
+    cp_calls = bench.step_pattern(cp)[0][1]
+    assert cp_calls[-1].tok_hi < 0 and bench.token_share_phase(cp_calls)
+    assert bench.pick_lanes(cp_calls) == 8 and bench.pick_call_sms(cp, cp_calls, 152) == 19
+    rc = W.ragged_cp()
+    rc_calls = bench.step_pattern(rc)[0][1]
+    assert bench.token_share_phase(rc_calls) and bench.pick_lanes(rc_calls) == 8
+    assert not bench.token_share_phase([C(0, 128, 0, 100), C(0, 128, 50, 200), C(0, 128, 200, -1)])
+    assert not bench.token_share_phase([C(0, 128, share=0), C(0, 128, share=0), C(0, 128, share=1)])
+    assert not bench.token_share_phase([C(0, 64, 0, 100), C(64, 128, 100, 200), C(0, 128, 200, -1)])
+    assert bench.token_share_phase([C(0, 128, 0, 100), C(0, 128, 100, 200), C(0, 128, 200, -1)])
 
 
 def test_per_request_ranges_count_their_own_tiles():

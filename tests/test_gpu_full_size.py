@@ -41,9 +41,8 @@ def _run_step(name):
     step = bench.Step(w, inp, DEV)
     step.run()
     torch.cuda.synchronize()
-    assert S.splash_workspace_status(step.ws) == 0
-    if step.ws_b is not None:
-        assert S.splash_workspace_status(step.ws_b) == 0
+    for ws in step.wss:
+        assert S.splash_workspace_status(ws) == 0
     return w, inp, step
 
 
