@@ -357,7 +357,7 @@ def token_share_phase(calls):
     """Whether a phase's calls are the token shares of one CP group: the same heads and
     requests, each call a different share of every request's tokens (scalar ranges that
     do not overlap, or distinct per-request shares).  Such calls read disjoint KV."""
-    if len(calls) < 3:
+    if len(calls) < 2:
         return False
     c0 = calls[0]
     if any(c.head_lo != c0.head_lo or c.head_hi != c0.head_hi or c.rows != c0.rows
@@ -848,7 +848,7 @@ def run_ours(args, world, rank, local):
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(w, inp, args.cpu_seconds)
-        if any(ph[0] == "decode" and lanes > 2 for ph, lanes in zip(step.phases, step.lanes)):
+        if any(ph[0] == "decode" and token_share_phase(ph[1]) for ph in step.phases):
             launch = ("the token shares of the CP group run at once, each call on its own stream "
                       "and workspace")
         elif any(ph[0] == "decode" and len(ph[1]) > 1 for ph in step.phases):

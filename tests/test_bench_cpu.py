@@ -95,11 +95,12 @@ def test_small_two_call_phases_get_half_the_sms():
     from layout_agnostic_paged_gb300 import workloads as W
     C = bench.CallSpec
     fh = W.full_heads()                       # 16 x 1024 tokens, 128 heads
-    shares = [C(0, 128, 0, 512), C(0, 128, 512, -1)]
-    assert [bench.call_cta_tiles(fh, c) for c in shares] == [16 * 4 * 2, 16 * 4 * 2]
-    assert bench.pick_call_sms(fh, shares, 152) == 76
-    assert bench.pick_call_sms(fh, shares, 100) == 0   # 128 CTA-tiles no longer fit in one wave
-    assert bench.pick_call_sms(fh, shares[:1], 152) == 0
+    halves = [C(0, 128, rows=list(range(8))), C(0, 128, rows=list(range(8, 16)))]
+    assert not bench.token_share_phase(halves)         # request subsets, not token shares
+    assert [bench.call_cta_tiles(fh, c) for c in halves] == [8 * 8 * 2, 8 * 8 * 2]
+    assert bench.pick_call_sms(fh, halves, 152) == 76
+    assert bench.pick_call_sms(fh, halves, 100) == 0   # 128 CTA-tiles no longer fit in one wave
+    assert bench.pick_call_sms(fh, halves[:1], 152) == 0
     hs = W.head_shard()                       # 16-head shards: one head group per call
     assert bench.call_cta_tiles(hs, C(0, 16)) == 128 * 32
     hs_calls = bench.step_pattern(hs)[0][1]
@@ -130,6 +131,11 @@ def test_cp_token_shares_run_at_once_on_an_even_sm_split():
     assert not bench.token_share_phase([C(0, 128, share=0), C(0, 128, share=0), C(0, 128, share=1)])
     assert not bench.token_share_phase([C(0, 64, 0, 100), C(64, 128, 100, 200), C(0, 128, 200, -1)])
     assert bench.token_share_phase([C(0, 128, 0, 100), C(0, 128, 100, 200), C(0, 128, 200, -1)])
+    gq = W.gqa()                              # two token shares: half the SMs each
+    gq_calls = bench.step_pattern(gq)[0][1]
+    assert bench.token_share_phase(gq_calls) and bench.pick_lanes(gq_calls) == 2
+    assert bench.pick_call_sms(gq, gq_calls, 152) == 76
+    assert not bench.token_share_phase(gq_calls[:1])
 
 
 def test_per_request_ranges_count_their_own_tiles():
