@@ -66,6 +66,10 @@ struct TcConfig {
     static constexpr int kThreads = 32 * (kFirstExtraProducer + kProducerWarps - 1);
     static constexpr int kPairs = NPAD == 64 ? 4 : 5;      // pair slots (ring)
     static constexpr int kRopes = NPAD == 16 ? 2 : 1;      // rope / P^T slots (ring)
+    // With two rope slots the next tile's rope slot is free long before its pairs' slots:
+    // the rope is then loaded first and contracted first, and only the last pair's MMAs
+    // follow the tile's last load.  With one, the slot holds P^T until the PV ends.
+    static constexpr bool kRopeFirst = kRopes > 1;
     static constexpr int kQBytes = 9 * NPAD * 128;
     static constexpr int kQOff = 0;
     static constexpr int kPairOff = kQOff + kQBytes;
@@ -312,6 +316,23 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                     // b % kProducerWarps, so the boxes that wait for the last PV of the
                     // previous tile (pair 3 and the rope) spread over all producer warps
                     const int bpp = 2 * pages_per_tile;  // boxes per pair
+                    // the rope block of page k is box 4 * bpp + k
+                    auto issue_rope = [&]() -> bool {
+                        const int g0 = 4 * bpp;
+                        if (owns_box(g0, pages_per_tile, pw)) {
+                            if (!warp_wait(&rope_empty[rs], rph ^ 1, abort_flag, status)) return false;
+                            if (lane == 0 && g0 % kProducerWarps == pw)
+                                mbar_arrive_expect_tx(&rope_full[rs], blk_bytes);
+                            if (my_pid >= 0 && (g0 + lane) % kProducerWarps == pw)
+                                tma_load_2d(sRope + rs * kColBlockBytes + lane * P * 128, &map_kv,
+                                            &rope_full[rs], 8 * 64, (my_pid * a.kv_heads + kvh) * P,
+                                            pol_kv);
+                            if (pw == g0 % kProducerWarps && lane == 0 && unsigned(ttr) < 3u)
+                                TRACE(6 + ttr * 3);
+                        }
+                        return true;
+                    };
+                    if (C::kRopeFirst && !issue_rope()) { ok = false; break; }
                     for (int jj = 0; jj < 4; ++jj) {
                         const int g0 = jj * bpp;
                         if (owns_box(g0, bpp, pw)) {
@@ -332,17 +353,7 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                     }
                     if (!ok) break;
                     if (pw == 0 && lane == 0 && unsigned(ttr) < 3u) TRACE(5 + ttr * 3);
-                    const int g0 = 4 * bpp;
-                    if (owns_box(g0, pages_per_tile, pw)) {
-                        if (!warp_wait(&rope_empty[rs], rph ^ 1, abort_flag, status)) { ok = false; break; }
-                        if (lane == 0 && g0 % kProducerWarps == pw)
-                            mbar_arrive_expect_tx(&rope_full[rs], blk_bytes);
-                        if (my_pid >= 0 && (g0 + lane) % kProducerWarps == pw)
-                            tma_load_2d(sRope + rs * kColBlockBytes + lane * P * 128, &map_kv,
-                                        &rope_full[rs], 8 * 64, (my_pid * a.kv_heads + kvh) * P, pol_kv);
-                        if (pw == g0 % kProducerWarps && lane == 0 && unsigned(ttr) < 3u)
-                            TRACE(6 + ttr * 3);
-                    }
+                    if (!C::kRopeFirst && !issue_rope()) { ok = false; break; }
                     ++ttr;
                     if (++rs == C::kRopes) { rs = 0; rph ^= 1; }
                 }
@@ -378,7 +389,23 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                     const bool first = (t == pc.t_lo), last = (t + 1 == pc.t_hi);
                     const int ps0 = ps;
                     if (lane == 0 && unsigned(ttr) < 3u) TRACE(13 + ttr * 5);
-                    // S^T = K_tile . Q^T over the 512 latent dims (pairs) ...
+                    // S^T = K_tile . Q^T over the 64 rope dims (first, when the rope is
+                    // loaded first) and the 512 latent dims (pairs)
+                    auto rope_mmas = [&](bool overwrite) -> bool {
+                        if (!mbar_wait(&rope_full[rs], rph, abort_flag, status)) return false;
+                        if (lane == 0 && unsigned(ttr) < 3u) TRACE(14 + ttr * 5);
+                        tc_fence_after();
+                        if (lane == 0) {
+                            const uint64_t da_r = dr0 + uint64_t(rs) * (kColBlockBytes >> 4);
+#pragma unroll
+                            for (int k4 = 0; k4 < 4; ++k4)
+                                mma_bf16_ss(s_tmem, da_r + ((k4 * 32) >> 4),
+                                            dq0 + ((8 * NPAD * 128 + k4 * 32) >> 4), idesc_qk,
+                                            (!overwrite || k4 > 0) ? 1u : 0u);
+                        }
+                        return true;
+                    };
+                    if (C::kRopeFirst && !rope_mmas(true)) { ok = false; break; }
                     for (int jj = 0; jj < 4; ++jj) {
                         if (!mbar_wait(&pair_full[ps], pph, abort_flag, status)) { ok = false; break; }
                         if (lane == 0 && ttr == 1) TRACE(51 + jj);
@@ -392,21 +419,13 @@ __global__ void __launch_bounds__(TcConfig<NPAD>::kThreads, 1)
                                 for (int k4 = 0; k4 < 4; ++k4)
                                     mma_bf16_ss(s_tmem, da_s + ((c2 * kColBlockBytes + k4 * 32) >> 4),
                                                 db_s + ((c2 * NPAD * 128 + k4 * 32) >> 4), idesc_qk,
-                                                (jj | c2 | k4) != 0);
+                                                (C::kRopeFirst || (jj | c2 | k4) != 0) ? 1u : 0u);
                         }
-                            if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
+                        if (++ps == C::kPairs) { ps = 0; pph ^= 1; }
                     }
                     if (!ok) break;
-                    // ... and the 64 rope dims
-                    if (!mbar_wait(&rope_full[rs], rph, abort_flag, status)) { ok = false; break; }
-                    if (lane == 0 && unsigned(ttr) < 3u) TRACE(14 + ttr * 5);
-                    tc_fence_after();
+                    if (!C::kRopeFirst && !rope_mmas(false)) { ok = false; break; }
                     if (lane == 0) {
-                        const uint64_t da_r = dr0 + uint64_t(rs) * (kColBlockBytes >> 4);
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4)
-                            mma_bf16_ss(s_tmem, da_r + ((k4 * 32) >> 4),
-                                        dq0 + ((8 * NPAD * 128 + k4 * 32) >> 4), idesc_qk, 1u);
                         tc_commit(s_full);
                         if (last) tc_commit(q_empty);
                         if (unsigned(ttr) < 3u) TRACE(15 + ttr * 5);
