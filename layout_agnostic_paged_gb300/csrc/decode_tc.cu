@@ -18,9 +18,10 @@
 // Roles (one CTA per SM, persistent over the split plan's pieces; 256 threads, or
 // 384 at N = 64 where two softmax warpgroups each own half of the heads):
 //   warp 0 and  TMA producers: Q of the piece, then per tile four 32 KB "pairs"
-//   the last    (latent column blocks 2j, 2j+1) and the 16 KB rope block, each page
-//   two warps   fetched through the block table (2D tiled loads, 128-byte swizzle);
-//               the boxes are dealt round-robin to the three warps
+//   the last    (latent column blocks 2j, 2j+1) and the 16 KB rope block (first, where
+//   two warps   there are two rope slots), each page fetched through the block table
+//               (2D tiled loads, 128-byte swizzle); the boxes are dealt round-robin to
+//               the three warps
 //   warp 1      TMEM allocation; its lane 0 alone walks the schedule and issues every
 //               MMA (no warp-wide votes or syncs on the path from a landed tile to
 //               its MMAs)
