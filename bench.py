@@ -372,9 +372,10 @@ def token_share_phase(calls):
 
 
 def pick_lanes(calls):
-    """Streams a decode phase's calls run on.  The token shares of a CP group run all at
-    once, as the group's ranks would, each call on its own stream; other multi-call
-    phases alternate between two streams."""
+    """Streams a decode phase's calls run on.  The token shares of a CP group run at once,
+    as the group's ranks would, each call on its own stream (those that find no free SMs
+    start as the first ones finish); other multi-call phases alternate between two
+    streams."""
     if token_share_phase(calls):
         return len(calls)
     return 2 if len(calls) > 1 else 1
@@ -382,14 +383,17 @@ def pick_lanes(calls):
 
 def pick_call_sms(w, calls, sms, ranges=None):
     """SM budget of each call of a phase (0: all).  The concurrent token shares of a CP
-    group split the SMs evenly.  A phase of several calls whose tiles each fill at most
-    one wave of the GPU would leave SMs idle while the other stream's call waits for
-    them; such calls each get half the SMs and run side by side (two ranks sharing one
-    GPU).  Larger calls, and a phase of one call, keep every SM."""
+    group each get 1/min(n, 4) of the SMs: four at a time of an eight-way group (a
+    quarter each; an eighth would leave SMs idle, as a 64-head call's CTAs come in pairs,
+    and measured slower on both CP workloads), two halves for two shares.  A phase of
+    several calls whose tiles each fill at most one wave of the GPU would leave SMs idle
+    while the other stream's call waits for them; such calls each get half the SMs and
+    run side by side (two ranks sharing one GPU).  Larger calls, and a phase of one call,
+    keep every SM."""
     if len(calls) < 2:
         return 0
     if token_share_phase(calls):
-        return sms // len(calls)
+        return sms // min(len(calls), 4)
     if all(call_cta_tiles(w, c, ranges) <= sms for c in calls):
         return sms // 2
     return 0
@@ -850,7 +854,7 @@ def run_ours(args, world, rank, local):
             cpu = cpu_baseline(w, inp, args.cpu_seconds)
         if any(ph[0] == "decode" and token_share_phase(ph[1]) for ph in step.phases):
             launch = ("the token shares of the CP group run at once, each call on its own stream "
-                      "and workspace")
+                      "and workspace (calls beyond the SM budget start as SMs free up)")
         elif any(ph[0] == "decode" and len(ph[1]) > 1 for ph in step.phases):
             launch = "calls of a decode phase alternate between two streams, one workspace each"
         else:

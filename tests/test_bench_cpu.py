@@ -114,7 +114,8 @@ def test_small_two_call_phases_get_half_the_sms():
 
 def test_cp_token_shares_run_at_once_on_an_even_sm_split():
     """The 8 token shares of a CP group read disjoint KV: they run as the group's ranks
-    would, all at once, each on its own stream with an eighth of the SMs.  The scalar
+    would, all at once, each on its own stream with a quarter of the SMs (four run, the
+    rest start as SMs free up).  The scalar
     shares of the long-context batch (the last one open-ended) and the per-request shares
     of the ragged batch both qualify; overlapping or repeated shares do not."""
     bench = _bench()
@@ -123,7 +124,7 @@ def test_cp_token_shares_run_at_once_on_an_even_sm_split():
     cp = W.cp_long()
     cp_calls = bench.step_pattern(cp)[0][1]
     assert cp_calls[-1].tok_hi < 0 and bench.token_share_phase(cp_calls)
-    assert bench.pick_lanes(cp_calls) == 8 and bench.pick_call_sms(cp, cp_calls, 152) == 19
+    assert bench.pick_lanes(cp_calls) == 8 and bench.pick_call_sms(cp, cp_calls, 152) == 38
     rc = W.ragged_cp()
     rc_calls = bench.step_pattern(rc)[0][1]
     assert bench.token_share_phase(rc_calls) and bench.pick_lanes(rc_calls) == 8
